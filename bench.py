@@ -1,0 +1,376 @@
+"""Benchmark of the MLA paged-decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = the whole hot path on one batch: split plan, attention over the
+pages, LSE combine (three kernels of libmla_gb300.so, called through the C ABI)
+on the named workload (default: the B=64, H=128 decode workload).  Inputs are
+seeded synthetic data (workloads/gen.py), resident in HBM before timing.
+
+Timing: W >= 3 untimed warm-up steps; then K steps, each bracketed by CUDA
+events on the launching stream, with a 512 MiB L2 flush (a buffer write)
+between steps outside the events; barrier + synchronize on both sides of the
+K steps; max over ranks.  Rank 0 prints one JSON line.
+
+Metric: TFLOP/s, counting 2*576 + 2*512 = 2176 flops per (query row, visible
+key); the line also carries KV GB/s (unique cache bytes read: 1152 B/token
+bf16, 596 B/token fp8 incl. scales) and the fraction of the roofline
+max(flops / tensor peak, KV bytes / HBM peak) for the step.
+
+--impl reference times the fp64 CPU oracle (the reference of this build) on
+a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import gen  # noqa: E402
+
+METRIC = "MLA decode TFLOP/s and KV GB/s at B=64,H=128 (1 GB300) + % of roofline"
+FLOP_PER_ROW_KEY = 2 * 576 + 2 * 512
+L2_FLUSH_BYTES = 512 << 20
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny: B=2 s_q=1 H=16 seqlens {37,130}, bf16 cache, page 64",
+    "decode": "decode: B=64 s_q=1 H=128 seqlens U[1024,4096], bf16 q and latent cache, page 64, scale 1/sqrt(192)",
+    "mtp": "MTP verify: B=128 s_q=2 (causal) H=128 seqlen 4096, bf16, page 64",
+    "long": "long skewed: B=16 s_q=1 H=128 lognormal seqlens (mean 3500, sigma 1) + one 65536, bf16, page 64",
+    "fp8": "fp8 cache: B=256 s_q=2 (causal) H=128 seqlen 2048, e4m3 cache + fp32 scale per token per 128-ch group",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def work_of(inp):
+    """(flops, kv_bytes) of one call: per row the visible keys, per request the
+    cache bytes of the tokens the longest row sees."""
+    flops = 0
+    kv_bytes = 0
+    per_tok = 596 if inp.kv_fp8 else 1152
+    for s in inp.seqlens.tolist():
+        for i in range(inp.s_q):
+            n = max(0, s - inp.s_q + i + 1)
+            flops += inp.heads * n * FLOP_PER_ROW_KEY
+        kv_bytes += max(0, s) * per_tok
+    return flops, kv_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reference_arm(args):
+    """The fp64 CPU oracle on a bounded sample of the workload, per step."""
+    import oracle
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    inp = gen.make_inputs(args.workload)
+    # sample: the first request(s), all of their rows, about a second of oracle work per step
+    R = inp.s_q * inp.heads
+    budget_flops = 3e9 * max(1, oracle.num_threads() // 4)
+    rows = []
+    flops = 0
+    for b in range(inp.batch):
+        s = int(inp.seqlens[b])
+        f = sum(inp.heads * max(0, s - inp.s_q + i + 1) for i in range(inp.s_q)) * FLOP_PER_ROW_KEY
+        if rows and flops + f > budget_flops:
+            break
+        rows.extend(range(b * R, (b + 1) * R))
+        flops += f
+    nreq = len(rows) // R
+    rows_t = torch.tensor(rows, dtype=torch.int64)
+    for _ in range(args.warmup):
+        oracle.mla_decode_inputs(inp, rows=rows_t)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mla_decode_inputs(inp, rows=rows_t)
+    dt = (time.perf_counter() - t0) / args.steps
+    tflops = flops / dt / 1e12
+    cores = oracle.num_threads()
+    sample = f"{nreq} request(s) x {R} rows of the {args.workload} workload per step ({flops/1e9:.2f} GFLOP)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, workloads/gen.py)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "sample": sample},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(inp, seconds: float = 12.0):
+    """Time the oracle on a bounded sample of the workload (rank 0, N=1)."""
+    import oracle
+    R = inp.s_q * inp.heads
+    rows, flops = [], 0
+    target = 2.5e9 * max(1, oracle.num_threads())  # ~ seconds of work on the host cores
+    for b in range(inp.batch):
+        s = int(inp.seqlens[b])
+        f = sum(inp.heads * max(0, s - inp.s_q + i + 1) for i in range(inp.s_q)) * FLOP_PER_ROW_KEY
+        if rows and flops + f > target:
+            break
+        rows.extend(range(b * R, (b + 1) * R))
+        flops += f
+    rows_t = torch.tensor(rows, dtype=torch.int64)
+    t0 = time.perf_counter()
+    oracle.mla_decode_inputs(inp, rows=rows_t)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)//R} request(s) x {R} rows ({flops/1e9:.2f} GFLOP) in {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=list(gen.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+
+    import mla_paged_decode_absorbed_gb300 as mla
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # each replica decodes its own batch of independent requests (weak scaling)
+    inp = gen.make_inputs(args.workload, seed=gen.workload_spec(args.workload).seed + 1000 * rank)
+    flops, kv_bytes = work_of(inp)
+    q = inp.q.to(dev)
+    kv = inp.kv.to(dev)
+    sc = inp.kv_scales.to(dev) if inp.kv_scales is not None else None
+    bt = inp.block_table.to(dev)
+    sl = inp.seqlens.to(dev)
+    dec = mla.MlaDecoder(inp.batch, inp.s_q, inp.heads, inp.num_pages, inp.max_pages_per_seq, kv_fp8=inp.kv_fp8,
+                         device=dev)
+    d = dec.desc
+    ws = dec.workspace
+    out = torch.empty((inp.batch, inp.s_q, inp.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((inp.batch, inp.s_q, inp.heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mla.mla_plan(d, sl, ws, stream)
+        ev_a.record(stream)
+        mla.mla_decode_attention(d, q, kv, sc, bt, sl, inp.s_q, inp.softmax_scale, out, lse, ws, stream)
+        ev_b.record(stream)
+        mla.mla_combine(d, out, lse, ws, stream)
+
+    ev_a = torch.cuda.Event(enable_timing=True)
+    ev_b = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = dec.device_error()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device error during warm-up: {mla.status_string(st)}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    clocks = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        ev_a, ev_b = k_a[i], k_b[i]
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(k_a, k_b)]
+    ms = sum(step_ms) / len(step_ms)
+    kms = sum(kern_ms) / len(kern_ms)
+    if world > 1:
+        t = torch.tensor([ms, kms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, kms = t.tolist()
+
+    # end to end through the C ABI call with host buffers: H2D of the step's
+    # inputs (q, block table, seqlens) from pinned memory, decode, D2H of out + lse
+    e2e = None
+    if not args.no_e2e:
+        q_h = inp.q.pin_memory()
+        bt_h = inp.block_table.pin_memory()
+        sl_h = inp.seqlens.pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(q_h, non_blocking=True)
+            bt.copy_(bt_h, non_blocking=True)
+            sl.copy_(sl_h, non_blocking=True)
+            mla.mla_decode(d, q, kv, sc, bt, sl, inp.s_q, inp.softmax_scale, out, lse, ws, stream)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e_s[i].record(stream)
+            e2e_step()
+            e_e[i].record(stream)
+        torch.cuda.synchronize()
+        ems = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = t.item()
+        h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+        st = dec.device_error()
+        if st != mla.MLA_OK:
+            raise RuntimeError(f"device error in e2e leg: {mla.status_string(st)}")
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    hbm_gbs, tflops_peak, tflops_sust, peak_src = load_peaks()
+    tflops = world * flops / (ms * 1e-3) / 1e12
+    kv_gbs = world * kv_bytes / (ms * 1e-3) / 1e9
+    t_roof = max(flops / (tflops_peak * 1e12), kv_bytes / (hbm_gbs * 1e9))
+    k_tflops = flops / (kms * 1e-3) / 1e12
+    k_gbs = kv_bytes / (kms * 1e-3) / 1e9
+    hbm_bound = kv_bytes / (hbm_gbs * 1e9) >= flops / (tflops_peak * 1e12)
+    if hbm_bound:
+        roof = {"kernel": "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>", "bound": "hbm",
+                "achieved": k_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": k_gbs / hbm_gbs,
+                "traffic": None, "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
+                "algorithmic_bytes_per_launch": kv_bytes}
+    else:
+        roof = {"kernel": "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>", "bound": "tensor",
+                "achieved": k_tflops, "peak": tflops_peak, "unit": "TFLOP/s", "frac": k_tflops / tflops_peak,
+                "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
+                "algorithmic_flops_per_launch": flops}
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if not inp.kv_fp8 else "bf16 (e4m3 cache)",
+        "data": "synthetic (seeded, workloads/gen.py)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "flushed between steps (512 MiB buffer write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "clusters": dec.num_clusters, "step": "plan + attention + combine kernels"},
+        "kv_gbs": kv_gbs, "pct_roofline": t_roof / (ms * 1e-3),
+        "decode_kernel_ms": kms, "decode_kernel_tflops": k_tflops, "decode_kernel_kv_gbs": k_gbs,
+        "roofline": roof,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) MLA paged-decode library, absorbed form.
+ *
+ * The operation (PaddleNLP issue #10157, section "Multi-head Latent Attention
+ * (MLA) 算子 / 总体概述": Data Load -> QK GEMM -> Softmax Update + R2S -> PV
+ * GEMM, with the decoder supporting num_token > 1; the verify step of
+ * "MTP 高效推理实现大批次加速 / draft token 验证阶段注意力计算优化" keeps the batch
+ * size and verifies every draft token in one pass; the matrix-absorption switch
+ * of the PaddleNLP best-practice digest, section 2.4.3,
+ * "--mla_use_matrix_absorption 1", runs the attention on the latent cache):
+ *
+ *   for request b, new token i < s_q, head h, with n = seqlen[b] - s_q + i + 1:
+ *     s_t  = softmax_scale * <q[b,i,h,0:576], K_t[0:576]>,  t < n
+ *     out[b,i,h,c] = sum_t softmax(s)_t * K_t[c],  c < 512
+ *     lse[b,i,h]   = ln sum_t exp(s_t)                  (natural log)
+ *   K_t is row t%64 of page block_table[b][t/64]; n <= 0 gives out 0, lse -inf.
+ *
+ * The split of each request's pages across SMs and the LSE merge of the pieces
+ * follow the cache partitioning of the same digest, section 1.4 ("Append
+ * Attention 优化", FLAGS_cascade_attention_max_partition_size).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to device memory of the
+ *     current CUDA device; the caller owns every buffer, the library allocates
+ *     nothing and keeps no state besides a per-device cache of launch limits.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on that stream and never synchronise the host, except
+ *     mla_get_device_error().
+ *   - Problems the host can see (bad sizes, NULL or misaligned pointers, short
+ *     workspace) return a negative mla_status and launch nothing.  Problems
+ *     only the device can see (a page id outside the pool, a seqlen beyond the
+ *     block table, a pipeline wait that timed out) set an error word in the
+ *     workspace, the kernels finish without trapping, and
+ *     mla_get_device_error() reports them.  Nothing aborts the process.
+ */
+#ifndef MLA_GB300_H_
+#define MLA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,    /* bad size, NULL or misaligned pointer, bad scale */
+  MLA_ERR_UNSUPPORTED = -2,    /* page_size != 64, d_qk != 576, d_v != 512, unknown kv dtype */
+  MLA_ERR_WORKSPACE = -3,      /* workspace NULL, misaligned or smaller than mla_workspace_size() */
+  MLA_ERR_LAUNCH = -4,         /* a kernel launch failed (no sm_103a device, bad configuration) */
+  MLA_ERR_DEVICE_BOUNDS = -5,  /* device saw a page id outside [0, num_pages) or seqlen outside [0, 64*max_pages] */
+  MLA_ERR_DEVICE_TIMEOUT = -6, /* a pipeline wait in the decode kernel exceeded its time limit */
+  MLA_ERR_CUDA = -7,           /* a CUDA runtime call failed */
+  MLA_ERR_DEVICE_RANGE = -8    /* fp8 cache: a scale with 448*|scale| > 65504 (outside the fp16 compute range) */
+} mla_status;
+
+typedef enum {
+  MLA_KV_BF16 = 0,     /* kv_pages: bf16 [num_pages, 64, 576]; MMAs in bf16 */
+  MLA_KV_FP8_E4M3 = 1  /* kv_pages: e4m3 bytes [num_pages, 64, 576] + kv_scales fp32 [num_pages, 64, 5];
+                          dequantised to fp16 in the load path and MMAs in fp16 (q is converted to
+                          fp16 per row with a power-of-two scale, so it cannot overflow) */
+} mla_kv_dtype;
+
+/* Problem description.  All fields are plain sizes; unset optional fields are 0. */
+typedef struct {
+  int32_t batch;              /* B >= 1 requests */
+  int32_t s_q;                /* new tokens per request, 1..16 (MTP verify uses > 1) */
+  int32_t num_heads;          /* H, 1..1024 */
+  int32_t num_pages;          /* pages in the KV pool, >= 1 */
+  int32_t max_pages_per_seq;  /* row length of block_table, >= 1 */
+  int32_t page_size;          /* must be 64 tokens */
+  int32_t d_qk;               /* must be 576 (512 latent + 64 RoPE) */
+  int32_t d_v;                /* must be 512 (the latent part of each KV row) */
+  int32_t kv_dtype;           /* mla_kv_dtype */
+  int32_t max_clusters;       /* optional cap on the number of 2-CTA clusters (0 = what the device holds) */
+  int32_t plan_overhead;      /* optional planner cost per (row block, request) in pages (0 = default 2) */
+  int32_t reserved[5];        /* must be 0 */
+} mla_desc;
+
+/*
+ * Bytes of device workspace mla_decode() needs for `desc` on a device with
+ * `num_sms` SMs (num_sms <= 0: query the current device).  The workspace holds
+ * the error word, the split plan and the fp32 partial outputs of split
+ * requests.  Returns 0 for an invalid desc.
+ */
+size_t mla_workspace_size(const mla_desc* desc, int num_sms);
+
+/*
+ * Number of 2-CTA clusters the decode kernel will use on the current device for
+ * `desc` (>= 1), or a negative mla_status.
+ */
+int mla_num_clusters(const mla_desc* desc);
+
+/*
+ * The whole hot path: mla_plan(), then mla_decode_attention(), then
+ * mla_combine(), in order on `stream`.
+ *
+ *   q            device, bf16 [B, s_q, H, 576], contiguous, 16-byte aligned
+ *   kv_pages     device, [num_pages, 64, 576] bf16 or e4m3 bytes, contiguous, 16-byte aligned
+ *   kv_scales    device, fp32 [num_pages, 64, 5] for MLA_KV_FP8_E4M3 (one scale per token per
+ *                channel group [0,128) [128,256) [256,384) [384,512) [512,576)); NULL for bf16
+ *   block_table  device, int32 [B, max_pages_per_seq]; entries at or past
+ *                ceil(seqlen/64) are never read
+ *   seqlens      device, int32 [B]; keys already in the cache for each request,
+ *                counting its s_q new tokens
+ *   s_q          must equal desc->s_q
+ *   softmax_scale  finite, > 0 (1/sqrt(192) for DeepSeek-style MLA)
+ *   out          device, bf16 [B, s_q, H, 512], 16-byte aligned (written)
+ *   lse          device, fp32 [B, s_q, H], natural log (written)
+ *   workspace    device, 256-byte aligned, >= mla_workspace_size(desc, 0) bytes
+ */
+mla_status mla_decode(const mla_desc* desc, const void* q, const void* kv_pages, const float* kv_scales,
+                      const int32_t* block_table, const int32_t* seqlens, int32_t s_q, float softmax_scale,
+                      void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 1 (split planner, one small kernel): reads seqlens on the device and
+ * writes the plan into the workspace.  Work units are (row block of 128 query
+ * rows, request) pairs ordered row-block-major; each costs ceil(n_max/64) + the
+ * plan overhead, where n_max is the visible-key count of the block's last row.
+ * Cluster c of G owns the cost range [c*W, (c+1)*W), W = ceil(total/G), and a
+ * unit whose pages cross a range boundary is split.  Also clears the error word.
+ */
+mla_status mla_plan(const mla_desc* desc, const int32_t* seqlens, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * Step 2 (attention over the pages, one kernel of 2-CTA clusters): needs the
+ * plan of mla_plan() in the same workspace.  Writes out/lse for requests that
+ * were not split, and fp32 partials (normalised output + lse per piece) in the
+ * workspace for requests that were.  Arguments as for mla_decode().
+ */
+mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void* kv_pages,
+                                const float* kv_scales, const int32_t* block_table, const int32_t* seqlens,
+                                int32_t s_q, float softmax_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * Step 3 (LSE-weighted combine, one kernel): for every split request,
+ *   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
+ * over its pieces, written to out (bf16) and lse.  Needs the plan and the
+ * partials of the two previous steps in the same workspace.
+ */
+mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * Synchronises `stream`, then reads the workspace error word written by the
+ * last mla_plan()/mla_decode_attention() on this workspace: MLA_OK,
+ * MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_DEVICE_RANGE (in
+ * that order of precedence when several happened), or MLA_ERR_CUDA if the copy
+ * itself failed.
+ */
+mla_status mla_get_device_error(const void* workspace, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* mla_status_string(int status);
+
+/* Byte offsets of the workspace regions (for tests and tools that inspect the
+ * plan).  The header is int32 words: [0] error bits, [1] W, [2] total cost,
+ * [3] units, [4] clusters, [5] plan overhead.  cl_first is int32 [clusters]
+ * (first unit each cluster touches), pre is int32 [units + 1] (cost prefix),
+ * lse_part fp32 [2*clusters, 128], o_part fp32 [2*clusters, 128, 512]. */
+typedef struct {
+  size_t header, cl_first, pre, lse_part, o_part, total;
+} mla_workspace_layout;
+mla_status mla_get_workspace_layout(const mla_desc* desc, int num_clusters, mla_workspace_layout* layout);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H_ */

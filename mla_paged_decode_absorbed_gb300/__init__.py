@@ -1,0 +1,243 @@
+"""Python binding of the GB300 MLA paged-decode library (absorbed form).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libmla_gb300.so`` (C ABI in ``include/mla.h``).  PyTorch supplies
+device memory and the current stream.  There is no CPU fallback: if the
+library cannot be loaded the calls raise.
+
+Functions mirror the C entry points: ``mla_workspace_size``, ``mla_plan``,
+``mla_decode_attention``, ``mla_combine``, ``mla_decode``,
+``mla_get_device_error``.  ``MlaDecoder`` bundles a descriptor and a cached
+workspace for repeated calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = -1
+MLA_ERR_UNSUPPORTED = -2
+MLA_ERR_WORKSPACE = -3
+MLA_ERR_LAUNCH = -4
+MLA_ERR_DEVICE_BOUNDS = -5
+MLA_ERR_DEVICE_TIMEOUT = -6
+MLA_ERR_CUDA = -7
+MLA_ERR_DEVICE_RANGE = -8
+
+MLA_KV_BF16 = 0
+MLA_KV_FP8_E4M3 = 1
+
+PAGE, D_QK, D_V = 64, 576, 512
+
+
+class MlaDesc(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("s_q", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("d_qk", ctypes.c_int32),
+        ("d_v", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("max_clusters", ctypes.c_int32),
+        ("plan_overhead", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
+    ]
+
+
+class MlaWorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "cl_first", "pre", "lse_part", "o_part", "total")]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library {LIB_PATH} is not built; run __graft_entry__.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+            dp = ctypes.POINTER(MlaDesc)
+            lib.mla_workspace_size.restype = sz
+            lib.mla_workspace_size.argtypes = [dp, ctypes.c_int]
+            lib.mla_num_clusters.restype = ctypes.c_int
+            lib.mla_num_clusters.argtypes = [dp]
+            lib.mla_plan.restype = ctypes.c_int
+            lib.mla_plan.argtypes = [dp, vp, vp, sz, vp]
+            lib.mla_decode_attention.restype = ctypes.c_int
+            lib.mla_decode_attention.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+            lib.mla_combine.restype = ctypes.c_int
+            lib.mla_combine.argtypes = [dp, vp, vp, vp, sz, vp]
+            lib.mla_decode.restype = ctypes.c_int
+            lib.mla_decode.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+            lib.mla_get_device_error.restype = ctypes.c_int
+            lib.mla_get_device_error.argtypes = [vp, vp]
+            lib.mla_status_string.restype = ctypes.c_char_p
+            lib.mla_status_string.argtypes = [ctypes.c_int]
+            lib.mla_get_workspace_layout.restype = ctypes.c_int
+            lib.mla_get_workspace_layout.argtypes = [dp, ctypes.c_int, ctypes.POINTER(MlaWorkspaceLayout)]
+            _lib = lib
+    return _lib
+
+
+def library():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _load()
+
+
+def status_string(status: int) -> str:
+    return _load().mla_status_string(int(status)).decode()
+
+
+def make_desc(batch: int, s_q: int, num_heads: int, num_pages: int, max_pages_per_seq: int,
+              kv_fp8: bool = False, max_clusters: int = 0, plan_overhead: int = 0) -> MlaDesc:
+    d = MlaDesc()
+    d.batch, d.s_q, d.num_heads = batch, s_q, num_heads
+    d.num_pages, d.max_pages_per_seq = num_pages, max_pages_per_seq
+    d.page_size, d.d_qk, d.d_v = PAGE, D_QK, D_V
+    d.kv_dtype = MLA_KV_FP8_E4M3 if kv_fp8 else MLA_KV_BF16
+    d.max_clusters, d.plan_overhead = max_clusters, plan_overhead
+    return d
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, what: str):
+    if status != MLA_OK:
+        raise MlaError(status, what)
+
+
+def mla_workspace_size(desc: MlaDesc, num_sms: int = 0) -> int:
+    return int(_load().mla_workspace_size(ctypes.byref(desc), int(num_sms)))
+
+
+def mla_num_clusters(desc: MlaDesc) -> int:
+    n = int(_load().mla_num_clusters(ctypes.byref(desc)))
+    _check(n if n < 0 else MLA_OK, "mla_num_clusters")
+    return n
+
+
+def mla_get_workspace_layout(desc: MlaDesc, num_clusters: int) -> MlaWorkspaceLayout:
+    lay = MlaWorkspaceLayout()
+    _check(_load().mla_get_workspace_layout(ctypes.byref(desc), int(num_clusters), ctypes.byref(lay)),
+           "mla_get_workspace_layout")
+    return lay
+
+
+def alloc_workspace(desc: MlaDesc, device=None) -> torch.Tensor:
+    n = mla_workspace_size(desc, 0)
+    if n == 0:
+        raise MlaError(MLA_ERR_INVALID_ARG, "mla_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_plan(desc: MlaDesc, seqlens: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    _check(_load().mla_plan(ctypes.byref(desc), _ptr(seqlens), _ptr(workspace), workspace.numel(),
+                            _stream(stream)), "mla_plan")
+
+
+def mla_decode_attention(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, softmax_scale: float,
+                         out, lse, workspace, stream=None) -> None:
+    _check(_load().mla_decode_attention(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table),
+                                        _ptr(seqlens), int(s_q), float(softmax_scale), _ptr(out), _ptr(lse),
+                                        _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mla_decode_attention")
+
+
+def mla_combine(desc: MlaDesc, out, lse, workspace, stream=None) -> None:
+    _check(_load().mla_combine(ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                               _stream(stream)), "mla_combine")
+
+
+def mla_decode(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, softmax_scale: float, out, lse,
+               workspace, stream=None) -> None:
+    """Raw call of the C ``mla_decode`` on caller-provided tensors."""
+    _check(_load().mla_decode(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table),
+                              _ptr(seqlens), int(s_q), float(softmax_scale), _ptr(out), _ptr(lse),
+                              _ptr(workspace), workspace.numel(), _stream(stream)), "mla_decode")
+
+
+def mla_get_device_error(workspace: torch.Tensor, stream=None) -> int:
+    return int(_load().mla_get_device_error(_ptr(workspace), _stream(stream)))
+
+
+def _expect(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+class MlaDecoder:
+    """Descriptor + workspace for repeated decode calls on one configuration."""
+
+    def __init__(self, batch: int, s_q: int, num_heads: int, num_pages: int, max_pages_per_seq: int,
+                 kv_fp8: bool = False, max_clusters: int = 0, plan_overhead: int = 0, device=None):
+        self.desc = make_desc(batch, s_q, num_heads, num_pages, max_pages_per_seq, kv_fp8, max_clusters,
+                              plan_overhead)
+        self.device = torch.device(device or "cuda")
+        with torch.cuda.device(self.device):
+            self.workspace = alloc_workspace(self.desc, self.device)
+            self.num_clusters = mla_num_clusters(self.desc)
+
+    def __call__(self, q: torch.Tensor, kv: torch.Tensor, block_table: torch.Tensor, seqlens: torch.Tensor,
+                 softmax_scale: float, kv_scales: Optional[torch.Tensor] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        d = self.desc
+        B, sq, H = d.batch, d.s_q, d.num_heads
+        _expect(q, "q", torch.bfloat16, (B, sq, H, D_QK))
+        if d.kv_dtype == MLA_KV_FP8_E4M3:
+            if kv.dtype == torch.float8_e4m3fn:
+                kv = kv.view(torch.uint8)
+            _expect(kv, "kv", torch.uint8, (d.num_pages, PAGE, D_QK))
+            _expect(kv_scales, "kv_scales", torch.float32, (d.num_pages, PAGE, 5))
+        else:
+            _expect(kv, "kv", torch.bfloat16, (d.num_pages, PAGE, D_QK))
+            if kv_scales is not None:
+                raise ValueError("kv_scales is only for the fp8 cache")
+        _expect(block_table, "block_table", torch.int32, (B, d.max_pages_per_seq))
+        _expect(seqlens, "seqlens", torch.int32, (B,))
+        if out is None:
+            out = torch.empty((B, sq, H, D_V), dtype=torch.bfloat16, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, sq, H), dtype=torch.float32, device=q.device)
+        _expect(out, "out", torch.bfloat16, (B, sq, H, D_V))
+        _expect(lse, "lse", torch.float32, (B, sq, H))
+        mla_decode(d, q, kv, kv_scales, block_table, seqlens, sq, softmax_scale, out, lse, self.workspace, stream)
+        return out, lse
+
+    def device_error(self, stream=None) -> int:
+        return mla_get_device_error(self.workspace, stream)

@@ -1,0 +1,514 @@
+// C ABI of the MLA paged-decode library (declared in include/mla.h): argument
+// validation, workspace layout, the split planner kernel, the LSE combine
+// kernel, tensor-map encoding and the launch sequence on the caller's stream.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "mla.h"
+#include "mla_internal.h"
+
+namespace mla_gb300 {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kCombineRowsPerCta = 16;
+constexpr int kCombineThreads = 256;
+
+// ------------------------------------------------------------------ planner
+// Cost of unit u (row block rb = u / B of request b = u % B): the pages the
+// block's last row can see, plus a fixed overhead for the unit's prologue and
+// epilogue.  seqlen outside [0, 64*max_pages] is clamped and flagged.
+__device__ __forceinline__ int unit_cost(const int32_t* seqlens, int u, int B, int s_q, int H, int R,
+                                         int max_pages, int ovh, int32_t* err) {
+  const int b = u % B, rb = u / B;
+  int seqlen = seqlens[b];
+  if (seqlen < 0 || seqlen > max_pages * kPage) {
+    atomicOr(err, kErrBounds);
+    seqlen = seqlen < 0 ? 0 : max_pages * kPage;
+  }
+  const int r_last = min(R, (rb + 1) * kRowsPerBlock) - 1;
+  int n = seqlen - s_q + r_last / H + 1;
+  n = n < 0 ? 0 : (n > seqlen ? seqlen : n);
+  return (n + kPage - 1) / kPage + ovh;
+}
+
+// One CTA: per-unit costs, their exclusive prefix sum `pre`, the per-cluster
+// budget W = ceil(total / G), and the first unit each cluster touches.
+__global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* seqlens, int B, int s_q, int H,
+                                                                int R, int U, int max_pages, int G, int ovh,
+                                                                int32_t* hdr, int32_t* cl_first, int32_t* pre) {
+  __shared__ int warp_sum[32];
+  __shared__ int s_W;
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) hdr[kHdrErr] = 0;
+  __syncthreads();
+  int32_t* err = hdr + kHdrErr;
+  const int chunk = (U + T - 1) / T;
+  const int u0 = min(U, tid * chunk), u1 = min(U, u0 + chunk);
+  int local = 0;
+  for (int u = u0; u < u1; ++u) local += unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
+  // block-wide exclusive scan of `local`
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = T / 32;
+    int v = lane < nw ? warp_sum[lane] : 0;
+    int vi = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, vi, d);
+      if (lane >= d) vi += x;
+    }
+    if (lane < nw) warp_sum[lane] = vi - v;  // exclusive warp offsets
+  }
+  __syncthreads();
+  int run = warp_sum[warp] + incl - local;
+  for (int u = u0; u < u1; ++u) {
+    pre[u] = run;
+    run += unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
+  }
+  if (u1 == U && u0 < u1) pre[U] = run;
+  if (U == 0 && tid == 0) pre[0] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    const int total = pre[U];
+    const int W = max(1, (total + G - 1) / G);
+    s_W = W;
+    hdr[kHdrW] = W;
+    hdr[kHdrTotal] = total;
+    hdr[kHdrUnits] = U;
+    hdr[kHdrClusters] = G;
+    hdr[kHdrOvh] = ovh;
+  }
+  for (int c = tid; c < G; c += T) cl_first[c] = U;
+  __syncthreads();
+  const int W = s_W;
+  for (int u = u0; u < u1; ++u) {
+    const int p0 = pre[u], p1 = pre[u + 1];
+    const int cf = (p0 + W - 1) / W, cl = (p1 + W - 1) / W - 1;
+    for (int c = cf; c <= cl && c < G; ++c) cl_first[c] = u;
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// CTA (c, y): the unit whose pages start in cluster c's range and continue
+// past it (at most one per cluster) is merged here, rows [16y, 16y+16) of it:
+//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k.
+__global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
+  const int c = blockIdx.x;
+  if (c + 1 >= a.clusters) return;
+  const int W = a.hdr[kHdrW];
+  const int u = a.cl_first[c + 1];
+  if (u >= a.U) return;
+  const int p0 = a.pre[u], p1 = a.pre[u + 1];
+  if (p1 - p0 - a.overhead <= 0) return;
+  const int first = p0 + a.overhead;
+  const int lo_c = c * W, hi_c = lo_c + W;
+  if (!(first >= lo_c && first < hi_c && p1 > hi_c)) return;
+  const int last = (p1 - 1) / W;
+  const int b = u % a.B, rb = u / a.B;
+  const int half = threadIdx.x >> 7;      // two rows per pass
+  const int t = threadIdx.x & 127;        // four channels per thread
+  for (int pass = 0; pass < kCombineRowsPerCta / 2; ++pass) {
+    const int L = blockIdx.y * kCombineRowsPerCta + pass * 2 + half;
+    const int r = rb * kRowsPerBlock + L;
+    if (r >= a.R) continue;
+    float mx = -INFINITY;
+    for (int cc = c; cc <= last; ++cc) {
+      const int slot = (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc;
+      mx = fmaxf(mx, a.lse_part[static_cast<size_t>(slot) * kRowsPerBlock + L]);
+    }
+    const size_t orow = static_cast<size_t>(b) * a.R + r;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lse_v = -INFINITY;
+    if (mx != -INFINITY) {
+      float wsum = 0.f;
+      for (int cc = c; cc <= last; ++cc) {
+        const int slot = (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc;
+        const float w = expf(a.lse_part[static_cast<size_t>(slot) * kRowsPerBlock + L] - mx);
+        const float4 o =
+            reinterpret_cast<const float4*>(a.o_part + (static_cast<size_t>(slot) * kRowsPerBlock + L) * kDv)[t];
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+        wsum += w;
+      }
+      const float inv = 1.f / wsum;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+      lse_v = mx + logf(wsum);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(a.out + orow * kDv)[t] = packed;
+    if (t == 0) a.lse[orow] = lse_v;
+  }
+}
+
+// ------------------------------------------------------------------ host helpers
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Dims {
+  int B, s_q, H, R, n_rb, U, P, maxp, ovh;
+  bool fp8;
+};
+
+mla_status check_desc(const mla_desc* d, Dims* out) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->page_size != kPage || d->d_qk != kDqk || d->d_v != kDv) return MLA_ERR_UNSUPPORTED;
+  if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+  if (d->batch < 1 || d->s_q < 1 || d->s_q > 16 || d->num_heads < 1 || d->num_heads > 1024) return MLA_ERR_INVALID_ARG;
+  if (d->num_pages < 1 || d->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
+  if (d->max_clusters < 0 || d->plan_overhead < 0) return MLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (d->reserved[i] != 0) return MLA_ERR_INVALID_ARG;
+  Dims x;
+  x.B = d->batch;
+  x.s_q = d->s_q;
+  x.H = d->num_heads;
+  x.R = d->s_q * d->num_heads;
+  x.n_rb = (x.R + kRowsPerBlock - 1) / kRowsPerBlock;
+  x.P = d->num_pages;
+  x.maxp = d->max_pages_per_seq;
+  x.ovh = d->plan_overhead > 0 ? d->plan_overhead : kDefaultOverhead;
+  x.fp8 = d->kv_dtype == MLA_KV_FP8_E4M3;
+  const int64_t U = static_cast<int64_t>(x.B) * x.n_rb;
+  // the plan's int32 cost prefix and page*64 token indices must not overflow
+  if (U * (static_cast<int64_t>(x.maxp) + x.ovh) >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(x.maxp) * kPage >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+  x.U = static_cast<int>(U);
+  if (out) *out = x;
+  return MLA_OK;
+}
+
+mla_workspace_layout layout_for(const Dims& x, int G) {
+  mla_workspace_layout l;
+  size_t off = 0;
+  l.header = off;
+  off += 256;
+  l.cl_first = off;
+  off += align256(sizeof(int32_t) * static_cast<size_t>(G));
+  l.pre = off;
+  off += align256(sizeof(int32_t) * (static_cast<size_t>(x.U) + 1));
+  l.lse_part = off;
+  off += align256(sizeof(float) * 2 * static_cast<size_t>(G) * kRowsPerBlock);
+  l.o_part = off;
+  off += sizeof(float) * 2 * static_cast<size_t>(G) * kRowsPerBlock * kDv;
+  l.total = align256(off);
+  return l;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int clusters_bf16 = 0, clusters_fp8 = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+mla_status device_info(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MLA_ERR_LAUNCH;  // built for sm_103a only
+    di.sms = prop.multiProcessorCount;
+    if (decode_max_active_clusters(false, &di.clusters_bf16) != cudaSuccess) return MLA_ERR_LAUNCH;
+    if (decode_max_active_clusters(true, &di.clusters_fp8) != cudaSuccess) return MLA_ERR_LAUNCH;
+    di.ready = true;
+  }
+  *info = di;
+  return MLA_OK;
+}
+
+int clusters_for(const mla_desc* d, const Dims& x, const DeviceInfo& di) {
+  int G = x.fp8 ? di.clusters_fp8 : di.clusters_bf16;
+  G = G < di.sms / 2 ? G : di.sms / 2;
+  if (d->max_clusters > 0 && d->max_clusters < G) G = d->max_clusters;
+  return G < 1 ? 1 : G;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [num_pages, 64, 576] cache viewed as a 3-D tensor; one box = 64 channels x 64
+// tokens of one page.  bf16 boxes are 128-byte rows with the 128-byte swizzle
+// the MMA descriptors expect; e4m3 boxes are plain 64-byte rows.
+mla_status make_kv_map(const void* kv, int num_pages, bool fp8, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  const cuuint64_t esz = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(kPage),
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[2] = {kDqk * esz, kDqk * esz * kPage};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
+struct Prepared {
+  Dims x;
+  DeviceInfo di;
+  int G;
+  mla_workspace_layout lay;
+  uint8_t* ws;
+};
+
+mla_status prepare(const mla_desc* d, void* workspace, size_t workspace_bytes, Prepared* p) {
+  mla_status st = check_desc(d, &p->x);
+  if (st != MLA_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  st = device_info(&p->di);
+  if (st != MLA_OK) return st;
+  p->G = clusters_for(d, p->x, p->di);
+  p->lay = layout_for(p->x, p->G);
+  if (workspace_bytes < p->lay.total) return MLA_ERR_WORKSPACE;
+  p->ws = static_cast<uint8_t*>(workspace);
+  return MLA_OK;
+}
+
+mla_status check_tensors(const Dims& x, const void* q, const void* kv, const float* kv_scales, const int32_t* bt,
+                         const int32_t* seqlens, const void* out, const float* lse) {
+  if (!q || !kv || !bt || !seqlens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(bt, 4) ||
+      !aligned(seqlens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (x.fp8) {
+    if (!kv_scales || !aligned(kv_scales, 16)) return MLA_ERR_INVALID_ARG;
+  } else if (kv_scales) {
+    return MLA_ERR_INVALID_ARG;
+  }
+  return MLA_OK;
+}
+
+mla_status launch_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH; }
+
+mla_status run_plan(const Prepared& p, const int32_t* seqlens, cudaStream_t stream) {
+  int32_t* hdr = reinterpret_cast<int32_t*>(p.ws + p.lay.header);
+  mla_plan_kernel<<<1, kPlanThreads, 0, stream>>>(seqlens, p.x.B, p.x.s_q, p.x.H, p.x.R, p.x.U, p.x.maxp, p.G,
+                                                  p.x.ovh, hdr, reinterpret_cast<int32_t*>(p.ws + p.lay.cl_first),
+                                                  reinterpret_cast<int32_t*>(p.ws + p.lay.pre));
+  return launch_status(cudaGetLastError());
+}
+
+mla_status run_attention(const Prepared& p, const void* q, const void* kv, const float* kv_scales,
+                         const int32_t* bt, const int32_t* seqlens, float scale, void* out, float* lse,
+                         cudaStream_t stream) {
+  CUtensorMap map;
+  mla_status st = make_kv_map(kv, p.x.P, p.x.fp8, &map);
+  if (st != MLA_OK) return st;
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv_scales = kv_scales;
+  a.block_table = bt;
+  a.seqlens = seqlens;
+  a.hdr = reinterpret_cast<const int32_t*>(p.ws + p.lay.header);
+  a.cl_first = reinterpret_cast<const int32_t*>(p.ws + p.lay.cl_first);
+  a.pre = reinterpret_cast<const int32_t*>(p.ws + p.lay.pre);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.o_part = reinterpret_cast<float*>(p.ws + p.lay.o_part);
+  a.lse_part = reinterpret_cast<float*>(p.ws + p.lay.lse_part);
+  a.err = reinterpret_cast<int32_t*>(p.ws + p.lay.header);
+  a.B = p.x.B;
+  a.s_q = p.x.s_q;
+  a.H = p.x.H;
+  a.R = p.x.R;
+  a.n_rb = p.x.n_rb;
+  a.U = p.x.U;
+  a.num_pages = p.x.P;
+  a.max_pages = p.x.maxp;
+  a.overhead = p.x.ovh;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_status(launch_decode(a, map, p.G, p.x.fp8, stream));
+}
+
+mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t stream) {
+  CombineArgs a;
+  a.hdr = reinterpret_cast<const int32_t*>(p.ws + p.lay.header);
+  a.cl_first = reinterpret_cast<const int32_t*>(p.ws + p.lay.cl_first);
+  a.pre = reinterpret_cast<const int32_t*>(p.ws + p.lay.pre);
+  a.o_part = reinterpret_cast<const float*>(p.ws + p.lay.o_part);
+  a.lse_part = reinterpret_cast<const float*>(p.ws + p.lay.lse_part);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.B = p.x.B;
+  a.R = p.x.R;
+  a.U = p.x.U;
+  a.clusters = p.G;
+  a.overhead = p.x.ovh;
+  dim3 grid(p.G, kRowsPerBlock / kCombineRowsPerCta);
+  mla_combine_kernel<<<grid, kCombineThreads, 0, stream>>>(a);
+  return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace mla_gb300
+
+using namespace mla_gb300;
+
+extern "C" {
+
+size_t mla_workspace_size(const mla_desc* desc, int num_sms) {
+  Dims x;
+  if (check_desc(desc, &x) != MLA_OK) return 0;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  }
+  int G = num_sms / 2;
+  if (desc->max_clusters > 0 && desc->max_clusters < G) G = desc->max_clusters;
+  if (G < 1) G = 1;
+  return layout_for(x, G).total;
+}
+
+int mla_num_clusters(const mla_desc* desc) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  DeviceInfo di;
+  st = device_info(&di);
+  if (st != MLA_OK) return st;
+  return clusters_for(desc, x, di);
+}
+
+mla_status mla_get_workspace_layout(const mla_desc* desc, int num_clusters, mla_workspace_layout* layout) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  if (num_clusters < 1 || !layout) return MLA_ERR_INVALID_ARG;
+  *layout = layout_for(x, num_clusters);
+  return MLA_OK;
+}
+
+mla_status mla_plan(const mla_desc* desc, const int32_t* seqlens, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  if (!seqlens || !aligned(seqlens, 4)) return MLA_ERR_INVALID_ARG;
+  Prepared p;
+  st = prepare(desc, workspace, workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  return run_plan(p, seqlens, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void* kv_pages, const float* kv_scales,
+                                const int32_t* block_table, const int32_t* seqlens, int32_t s_q,
+                                float softmax_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  if (s_q != desc->s_q || !std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  st = check_tensors(x, q, kv_pages, kv_scales, block_table, seqlens, out, lse);
+  if (st != MLA_OK) return st;
+  Prepared p;
+  st = prepare(desc, workspace, workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  return run_attention(p, q, kv_pages, kv_scales, block_table, seqlens, softmax_scale, out, lse,
+                       static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
+  Prepared p;
+  st = prepare(desc, workspace, workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  return run_combine(p, out, lse, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_decode(const mla_desc* desc, const void* q, const void* kv_pages, const float* kv_scales,
+                      const int32_t* block_table, const int32_t* seqlens, int32_t s_q, float softmax_scale,
+                      void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  if (s_q != desc->s_q || !std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  st = check_tensors(x, q, kv_pages, kv_scales, block_table, seqlens, out, lse);
+  if (st != MLA_OK) return st;
+  Prepared p;
+  st = prepare(desc, workspace, workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_plan(p, seqlens, s);
+  if (st != MLA_OK) return st;
+  st = run_attention(p, q, kv_pages, kv_scales, block_table, seqlens, softmax_scale, out, lse, s);
+  if (st != MLA_OK) return st;
+  return run_combine(p, out, lse, s);
+}
+
+mla_status mla_get_device_error(const void* workspace, void* stream) {
+  if (!workspace || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  int32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (word & kErrTimeout) return MLA_ERR_DEVICE_TIMEOUT;
+  if (word & kErrBounds) return MLA_ERR_DEVICE_BOUNDS;
+  if (word & kErrRange) return MLA_ERR_DEVICE_RANGE;
+  return MLA_OK;
+}
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MLA_ERR_LAUNCH: return "kernel launch failed";
+    case MLA_ERR_DEVICE_BOUNDS: return "device saw a page id or seqlen out of bounds";
+    case MLA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case MLA_ERR_CUDA: return "CUDA runtime call failed";
+    case MLA_ERR_DEVICE_RANGE: return "fp8 cache scale outside the fp16 compute range";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -55,6 +55,14 @@ class Plan:
     def units(self) -> int:
         return len(self.tiles)
 
+    def first_unit(self, c: int) -> int:
+        """The unit containing cost point c*W (units if the range is past the end)."""
+        x = c * self.W
+        for u in range(self.units):
+            if self.pre[u] <= x < self.pre[u + 1]:
+                return u
+        return self.units
+
     def pieces(self, c: int) -> List[Piece]:
         """Segments cluster c processes, in order."""
         lo_c, hi_c = c * self.W, (c + 1) * self.W

@@ -1,0 +1,184 @@
+"""Host-side checks that need no GPU: the C ABI library builds, loads and
+exports every symbol include/mla.h declares; host validation returns the
+documented status codes without touching the device; and the reference split
+plan has the properties the kernels rely on."""
+import ctypes
+import os
+import random
+import re
+import subprocess
+
+import pytest
+
+import mla_paged_decode_absorbed_gb300 as mla
+from mla_paged_decode_absorbed_gb300 import build as mla_build
+from oracle import plan_ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla_build.build()
+    return mla.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s*(mla_[a-z_]+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for need in ("mla_decode", "mla_plan", "mla_decode_attention", "mla_combine", "mla_workspace_size",
+                 "mla_get_device_error", "mla_status_string", "mla_num_clusters", "mla_get_workspace_layout"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", mla.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def _desc(**kw):
+    base = dict(batch=2, s_q=1, num_heads=16, num_pages=4, max_pages_per_seq=3)
+    base.update(kw)
+    return mla.make_desc(**base)
+
+
+def test_workspace_size_is_host_only(lib):
+    d = _desc()
+    n = mla.mla_workspace_size(d, 152)
+    lay = mla.mla_get_workspace_layout(d, 76)
+    assert n == lay.total and n % 256 == 0
+    assert lay.o_part >= lay.lse_part >= lay.pre >= lay.cl_first >= lay.header
+    assert lay.total - lay.o_part >= 2 * 76 * 128 * 512 * 4
+    # capping clusters shrinks the partial buffers
+    assert mla.mla_workspace_size(_desc(max_clusters=4), 152) < n
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("page_size", 32, mla.MLA_ERR_UNSUPPORTED),
+    ("d_qk", 512, mla.MLA_ERR_UNSUPPORTED),
+    ("d_v", 576, mla.MLA_ERR_UNSUPPORTED),
+    ("kv_dtype", 7, mla.MLA_ERR_UNSUPPORTED),
+    ("batch", 0, mla.MLA_ERR_INVALID_ARG),
+    ("s_q", 0, mla.MLA_ERR_INVALID_ARG),
+    ("s_q", 17, mla.MLA_ERR_INVALID_ARG),
+    ("num_heads", 0, mla.MLA_ERR_INVALID_ARG),
+    ("num_pages", 0, mla.MLA_ERR_INVALID_ARG),
+    ("max_clusters", -1, mla.MLA_ERR_INVALID_ARG),
+])
+def test_bad_descriptor_is_rejected_before_any_launch(lib, field, value, status):
+    d = _desc()
+    setattr(d, field, value)
+    assert lib.mla_workspace_size(ctypes.byref(d), 152) == 0
+    fake = 1 << 20  # never dereferenced: validation fails first
+    rc = lib.mla_decode(ctypes.byref(d), fake, fake, None, fake, fake, d.s_q, 0.07, fake, fake, fake, 1 << 30, None)
+    assert rc == status
+
+
+def test_reserved_fields_must_be_zero(lib):
+    d = _desc()
+    d.reserved[2] = 1
+    assert lib.mla_decode(ctypes.byref(d), 256, 256, None, 256, 256, 1, 0.07, 256, 256, 256, 1 << 30, None) \
+        == mla.MLA_ERR_INVALID_ARG
+
+
+def test_pointer_and_scalar_validation(lib):
+    d = _desc()
+    ok = 1 << 20
+    args = dict(q=ok, kv=ok, sc=None, bt=ok, sl=ok, s_q=1, scale=0.07, out=ok, lse=ok, ws=ok)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return lib.mla_decode(ctypes.byref(d), a["q"], a["kv"], a["sc"], a["bt"], a["sl"], a["s_q"], a["scale"],
+                              a["out"], a["lse"], a["ws"], 1 << 30, None)
+
+    assert call(q=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(q=ok + 8) == mla.MLA_ERR_INVALID_ARG          # q must be 16-byte aligned
+    assert call(kv=ok + 2) == mla.MLA_ERR_INVALID_ARG
+    assert call(lse=ok + 2) == mla.MLA_ERR_INVALID_ARG
+    assert call(sc=ok) == mla.MLA_ERR_INVALID_ARG              # scales only with the fp8 cache
+    assert call(s_q=2) == mla.MLA_ERR_INVALID_ARG              # must match the descriptor
+    assert call(scale=0.0) == mla.MLA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == mla.MLA_ERR_INVALID_ARG
+    assert call(ws=None) == mla.MLA_ERR_WORKSPACE
+    assert call(ws=ok + 16) == mla.MLA_ERR_WORKSPACE           # workspace must be 256-byte aligned
+    d8 = _desc(kv_fp8=True)
+    assert lib.mla_decode(ctypes.byref(d8), ok, ok, None, ok, ok, 1, 0.07, ok, ok, ok, 1 << 30, None) \
+        == mla.MLA_ERR_INVALID_ARG                             # fp8 needs scales
+    for code in range(-8, 1):
+        assert lib.mla_status_string(code).decode() != "unknown status"
+
+
+# ------------------------------------------------------------------ plan properties
+def _check_plan(plan):
+    covered = {}
+    slots = set()
+    for c in range(plan.G):
+        for p in plan.pieces(c):
+            if plan.tiles[p.unit] == 0:
+                covered.setdefault(p.unit, []).append(("empty", c))
+                continue
+            assert 0 <= p.page_lo < p.page_hi <= plan.tiles[p.unit]
+            covered.setdefault(p.unit, []).append((p.page_lo, p.page_hi, c, p.split, p.slot))
+            if p.split:
+                assert p.slot not in slots
+                assert p.slot in (2 * c, 2 * c + 1)
+                slots.add(p.slot)
+    combined = {}
+    for c in range(plan.G):
+        r = plan.combine_unit(c)
+        if r is not None:
+            u, pieces = r
+            assert u not in combined
+            combined[u] = pieces
+    for u in range(plan.units):
+        segs = covered.get(u, [])
+        if plan.tiles[u] == 0:
+            assert len(segs) == 1
+            continue
+        segs.sort()
+        assert segs[0][0] == 0 and segs[-1][1] == plan.tiles[u]
+        for a, b in zip(segs, segs[1:]):
+            assert a[1] == b[0]
+        if len(segs) == 1:
+            assert not segs[0][3] and u not in combined
+        else:
+            assert all(s[3] for s in segs)
+            assert sorted((s[2], s[4]) for s in segs) == sorted(combined[u])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_reference_plan_covers_every_page_once(seed):
+    rng = random.Random(seed)
+    B = rng.randint(1, 40)
+    s_q = rng.choice([1, 1, 2, 3, 5])
+    H = rng.choice([16, 20, 64, 128, 256])
+    maxp = rng.randint(1, 80)
+    seqlens = [rng.choice([0, 1, 63, 64, 65, rng.randint(0, maxp * 64)]) for _ in range(B)]
+    G = rng.randint(1, 80)
+    ovh = rng.choice([1, 2, 4])
+    _check_plan(plan_ref.make_plan(seqlens, s_q, H, maxp, G, ovh))
+
+
+def test_reference_plan_on_named_workloads():
+    from workloads import gen
+    for name in ("tiny", "decode", "long"):
+        inp = gen.make_inputs(name) if name == "tiny" else None
+        if inp is None:
+            import torch
+            g = torch.Generator("cpu").manual_seed(gen.workload_spec(name).seed)
+            sl = gen._seqlens_for(name, gen.workload_spec(name).batch, g).tolist()
+            maxp = max((s + 63) // 64 for s in sl)
+            plan = plan_ref.make_plan(sl, 1, 128, maxp, 76, 2)
+        else:
+            plan = plan_ref.make_plan(inp.seqlens.tolist(), 1, 16, inp.max_pages_per_seq, 76, 2)
+        _check_plan(plan)
