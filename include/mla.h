@@ -154,6 +154,29 @@ mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* worksp
  */
 mla_status mla_get_device_error(const void* workspace, void* stream);
 
+/*
+ * mla_decode() for callers that cannot allocate device memory at call time
+ * (serving loops and plugin hosts that reserve all memory up front and forbid
+ * allocation afterwards; C callers that own only their inputs and outputs).
+ * The pages have no counterpart: this is a packaging variant of mla_decode().
+ *
+ * Arguments as for mla_decode(), without the workspace.  The scratch is a
+ * fixed 40 MiB array inside the library, held on every GPU that loads this
+ * part of the library until the process exits; the call allocates nothing.
+ * The first call on a device looks up the array's device address (make it
+ * before any stream capture).  The call uses at most 76 two-CTA clusters; a
+ * problem whose plan and partials need more than 40 MiB (more than about
+ * 500,000 (row block, request) units) returns MLA_ERR_WORKSPACE and launches
+ * nothing.
+ * All calls share the array: calls that overlap on the GPU race, so serialise
+ * them.  With check_device_error != 0 the call synchronises `stream` and
+ * returns the device error status (as mla_get_device_error()); otherwise it
+ * returns without synchronising.
+ */
+mla_status mla_decode_noalloc(const mla_desc* desc, const void* q, const void* kv_pages, const float* kv_scales,
+                              const int32_t* block_table, const int32_t* seqlens, int32_t s_q, float softmax_scale,
+                              void* out, float* lse, int check_device_error, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* mla_status_string(int status);
 

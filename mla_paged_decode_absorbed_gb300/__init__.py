@@ -241,3 +241,25 @@ class MlaDecoder:
 
     def device_error(self, stream=None) -> int:
         return mla_get_device_error(self.workspace, stream)
+
+
+def noalloc_function():
+    """The C ``mla_decode_noalloc`` with its argument types declared."""
+    fn = _load().mla_decode_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(MlaDesc)] + [ctypes.c_void_p] * 5 + [ctypes.c_int32, ctypes.c_float,
+                                                                       ctypes.c_void_p, ctypes.c_void_p,
+                                                                       ctypes.c_int, ctypes.c_void_p]
+    return fn
+
+
+def mla_decode_noalloc(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, softmax_scale: float,
+                       out, lse, check_device_error: bool = False, stream=None) -> int:
+    """Raw call of the C ``mla_decode_noalloc`` (scratch inside the library,
+    no workspace argument, no device allocation).  Returns the status when
+    ``check_device_error`` is set (the call then synchronises the stream)."""
+    st = noalloc_function()(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table), _ptr(seqlens), int(s_q),
+            float(softmax_scale), _ptr(out), _ptr(lse), 1 if check_device_error else 0, _stream(stream))
+    if st not in (MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_RANGE):
+        raise MlaError(st, "mla_decode_noalloc")
+    return st
