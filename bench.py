@@ -134,6 +134,48 @@ def dist_env():
     return world, rank, local
 
 
+def replica_inputs(workload: str, rank: int):
+    """Each data-parallel replica decodes its own independent batch of the
+    same workload (weak scaling): same recipe, seed offset by the rank."""
+    return gen.make_inputs(workload, seed=gen.workload_spec(workload).seed + 1000 * rank)
+
+
+def max_over_ranks(values, device):
+    """Element-wise MAX of per-rank timings (a no-op without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def _request_flops(inp, b):
+    s = int(inp.seqlens[b])
+    return sum(inp.heads * max(0, s - inp.s_q + i + 1) for i in range(inp.s_q)) * FLOP_PER_ROW_KEY
+
+
+def oracle_sample(inp, seconds: float):
+    """Rows of the first requests of the workload (all their heads and tokens)
+    sized, from a one-request calibration run, to about `seconds` of oracle
+    work on the host cores; the whole batch when it takes less."""
+    import oracle
+    R = inp.s_q * inp.heads
+    first = torch.arange(0, R, dtype=torch.int64)
+    t0 = time.perf_counter()
+    oracle.mla_decode_inputs(inp, rows=first)
+    rate = _request_flops(inp, 0) / max(time.perf_counter() - t0, 1e-6)
+    budget = rate * seconds
+    rows, flops = [], 0
+    for b in range(inp.batch):
+        f = _request_flops(inp, b)
+        if rows and flops + f > budget:
+            break
+        rows.extend(range(b * R, (b + 1) * R))
+        flops += f
+    return torch.tensor(rows, dtype=torch.int64), flops, len(rows) // R
+
+
 def reference_arm(args):
     """The fp64 CPU oracle on a bounded sample of the workload, per step."""
     import oracle
@@ -141,20 +183,8 @@ def reference_arm(args):
     if rank != 0:
         return
     inp = gen.make_inputs(args.workload)
-    # sample: the first request(s), all of their rows, about a second of oracle work per step
     R = inp.s_q * inp.heads
-    budget_flops = 3e9 * max(1, oracle.num_threads() // 4)
-    rows = []
-    flops = 0
-    for b in range(inp.batch):
-        s = int(inp.seqlens[b])
-        f = sum(inp.heads * max(0, s - inp.s_q + i + 1) for i in range(inp.s_q)) * FLOP_PER_ROW_KEY
-        if rows and flops + f > budget_flops:
-            break
-        rows.extend(range(b * R, (b + 1) * R))
-        flops += f
-    nreq = len(rows) // R
-    rows_t = torch.tensor(rows, dtype=torch.int64)
+    rows_t, flops, nreq = oracle_sample(inp, 2.0)   # about 2 s of host work per step
     for _ in range(args.warmup):
         oracle.mla_decode_inputs(inp, rows=rows_t)
     t0 = time.perf_counter()
@@ -163,7 +193,8 @@ def reference_arm(args):
     dt = (time.perf_counter() - t0) / args.steps
     tflops = flops / dt / 1e12
     cores = oracle.num_threads()
-    sample = f"{nreq} request(s) x {R} rows of the {args.workload} workload per step ({flops/1e9:.2f} GFLOP)"
+    sample = (f"{nreq} of {inp.batch} requests x {R} rows of the {args.workload} workload per step "
+              f"({flops/1e9:.2f} GFLOP)")
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
@@ -176,24 +207,20 @@ def reference_arm(args):
 
 
 def cpu_baseline(inp, seconds: float = 12.0):
-    """Time the oracle on a bounded sample of the workload (rank 0, N=1)."""
+    """Time the oracle on a bounded sample of the workload (rank 0, N=1):
+    about `seconds` of host work; a sample smaller than that is repeated."""
     import oracle
     R = inp.s_q * inp.heads
-    rows, flops = [], 0
-    target = 2.5e9 * max(1, oracle.num_threads())  # ~ seconds of work on the host cores
-    for b in range(inp.batch):
-        s = int(inp.seqlens[b])
-        f = sum(inp.heads * max(0, s - inp.s_q + i + 1) for i in range(inp.s_q)) * FLOP_PER_ROW_KEY
-        if rows and flops + f > target:
+    rows_t, flops, nreq = oracle_sample(inp, seconds)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.mla_decode_inputs(inp, rows=rows_t)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.8 * seconds or reps >= 20:
             break
-        rows.extend(range(b * R, (b + 1) * R))
-        flops += f
-    rows_t = torch.tensor(rows, dtype=torch.int64)
-    t0 = time.perf_counter()
-    oracle.mla_decode_inputs(inp, rows=rows_t)
-    dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{len(rows)//R} request(s) x {R} rows ({flops/1e9:.2f} GFLOP) in {dt:.1f} s"}
+    return {"value": reps * flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{nreq} of {inp.batch} requests x {R} rows ({flops/1e9:.2f} GFLOP), run {reps}x in {dt:.1f} s"}
 
 
 def main():
@@ -222,7 +249,7 @@ def main():
     dev = torch.device("cuda", local)
 
     # each replica decodes its own batch of independent requests (weak scaling)
-    inp = gen.make_inputs(args.workload, seed=gen.workload_spec(args.workload).seed + 1000 * rank)
+    inp = replica_inputs(args.workload, rank)
     flops, kv_bytes = work_of(inp)
     q = inp.q.to(dev)
     kv = inp.kv.to(dev)
@@ -280,10 +307,7 @@ def main():
     kern_ms = [a.elapsed_time(b) for a, b in zip(k_a, k_b)]
     ms = sum(step_ms) / len(step_ms)
     kms = sum(kern_ms) / len(kern_ms)
-    if world > 1:
-        t = torch.tensor([ms, kms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, kms = t.tolist()
+    ms, kms = max_over_ranks([ms, kms], dev)
 
     # end to end through the C ABI call with host buffers: H2D of the step's
     # inputs (q, block table, seqlens) from pinned memory, decode, D2H of out + lse
@@ -315,10 +339,7 @@ def main():
             e_e[i].record(stream)
         torch.cuda.synchronize()
         ems = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = t.item()
+        ems = max_over_ranks([ems], dev)[0]
         h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
         d2h = out_h.numel() * 2 + lse_h.numel() * 4
         e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

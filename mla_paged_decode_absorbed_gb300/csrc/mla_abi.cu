@@ -18,7 +18,7 @@ namespace mla_gb300 {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kCombineRowsPerCta = 16;
+constexpr int kCombineRowsPerCta = 2;
 constexpr int kCombineThreads = 256;
 
 // ------------------------------------------------------------------ planner
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
 
 // ------------------------------------------------------------------ combine
 // CTA (c, y): the unit whose pages start in cluster c's range and continue
-// past it (at most one per cluster) is merged here, rows [16y, 16y+16) of it:
+// past it (at most one per cluster) is merged here, rows [2y, 2y+2) of it:
 //   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k.
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
   const int c = blockIdx.x;
@@ -121,48 +121,48 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   if (!(first >= lo_c && first < hi_c && p1 > hi_c)) return;
   const int last = (p1 - 1) / W;
   const int b = u % a.B, rb = u / a.B;
-  const int half = threadIdx.x >> 7;      // two rows per pass
-  const int t = threadIdx.x & 127;        // four channels per thread
-  for (int pass = 0; pass < kCombineRowsPerCta / 2; ++pass) {
-    const int L = blockIdx.y * kCombineRowsPerCta + pass * 2 + half;
-    const int r = rb * kRowsPerBlock + L;
-    if (r >= a.R) continue;
-    float mx = -INFINITY;
-    for (int cc = c; cc <= last; ++cc) {
-      const int slot = (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc;
-      mx = fmaxf(mx, a.lse_part[static_cast<size_t>(slot) * kRowsPerBlock + L]);
-    }
-    const size_t orow = static_cast<size_t>(b) * a.R + r;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse_v = -INFINITY;
-    if (mx != -INFINITY) {
-      float wsum = 0.f;
-      for (int cc = c; cc <= last; ++cc) {
-        const int slot = (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc;
-        const float w = expf(a.lse_part[static_cast<size_t>(slot) * kRowsPerBlock + L] - mx);
-        const float4 o =
-            reinterpret_cast<const float4*>(a.o_part + (static_cast<size_t>(slot) * kRowsPerBlock + L) * kDv)[t];
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
-        wsum += w;
-      }
-      const float inv = 1.f / wsum;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-      lse_v = mx + logf(wsum);
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(a.out + orow * kDv)[t] = packed;
-    if (t == 0) a.lse[orow] = lse_v;
+  const int L = blockIdx.y * kCombineRowsPerCta + (threadIdx.x >> 7);  // one row per 128 threads
+  const int t = threadIdx.x & 127;                                      // four channels per thread
+  const int r = rb * kRowsPerBlock + L;
+  if (r >= a.R) return;
+  // one pass over the pieces with a running max (pieces are independent, so
+  // their loads overlap); rows no piece saw keep lse = -inf and a zero output
+  float mx = -INFINITY, wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int cc = c; cc <= last; ++cc) {
+    const int slot = (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc;
+    const float lk = a.lse_part[static_cast<size_t>(slot) * kRowsPerBlock + L];
+    const float4 o =
+        reinterpret_cast<const float4*>(a.o_part + (static_cast<size_t>(slot) * kRowsPerBlock + L) * kDv)[t];
+    if (lk == -INFINITY) continue;
+    const float m_new = fmaxf(mx, lk);
+    const float scale_old = expf(mx - m_new);  // 0 when mx is -inf
+    const float w = expf(lk - m_new);
+    acc.x = acc.x * scale_old + w * o.x;
+    acc.y = acc.y * scale_old + w * o.y;
+    acc.z = acc.z * scale_old + w * o.z;
+    acc.w = acc.w * scale_old + w * o.w;
+    wsum = wsum * scale_old + w;
+    mx = m_new;
   }
+  float lse_v = -INFINITY;
+  if (wsum > 0.f) {
+    const float inv = 1.f / wsum;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    lse_v = mx + logf(wsum);
+  }
+  const size_t orow = static_cast<size_t>(b) * a.R + r;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(a.out + orow * kDv)[t] = packed;
+  if (t == 0) a.lse[orow] = lse_v;
 }
 
 // ------------------------------------------------------------------ host helpers

@@ -232,59 +232,99 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      SegIter it = it0;
-      Seg s;
-      int stage = 0;
-      uint32_t ph = 0;
-      int last_par[kFp8 ? C::kF8Stages : C::kStages];
-      for (int i = 0; i < (kFp8 ? C::kF8Stages : C::kStages); ++i) last_par[i] = -1;
-      bool ok = true;
-      const uint32_t bytes = kFp8 ? (uint32_t)(nbox * kBoxFp8 + kScaleBytes) : (uint32_t)(nbox * kBoxBf16);
-      while (ok && it.next(s)) {
-        if (s.empty) continue;
-        const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
-        for (int p = s.page_lo; p < s.page_hi; ++p) {
-          uint64_t* empty_bar = kFp8 ? &bars->f8_empty[stage] : &bars->kv_empty[stage];
-          uint64_t* full_bar = kFp8 ? &bars->f8_full[stage] : &bars->kv_full[stage];
-          if (!mbar_wait(smem_u32(empty_bar), ph ^ 1u, abort_flag)) {
-            ok = false;
-            if (!*abort_flag) signal_abort(bars, a.err, peer);
+    // The whole warp walks the segments; lane 0 waits and issues the copies.
+    // Page ids are read 32 at a time (one per lane) and shuffled out, so the
+    // block-table read is off the per-page critical path.
+    SegIter it = it0;
+    Seg s;
+    int stage = 0;
+    uint32_t ph = 0;
+    int last_par[kFp8 ? C::kF8Stages : C::kStages];
+    for (int i = 0; i < (kFp8 ? C::kF8Stages : C::kStages); ++i) last_par[i] = -1;
+    bool ok = true;
+    const uint32_t bytes = kFp8 ? (uint32_t)(nbox * kBoxFp8 + kScaleBytes) : (uint32_t)(nbox * kBoxBf16);
+    // L2 prefetch of a segment's Q rows (one request's block of <= 128 rows is
+    // contiguous), so the softmax warps' Q loads at the segment start hit L2.
+    auto prefetch_q = [&](const Seg& sg) {
+      if (lane != 0 || sg.empty) return;
+      const int r0 = sg.rb * kRowsPerBlock;
+      const int rows = min(kRowsPerBlock, a.R - r0);
+      const uint8_t* base = reinterpret_cast<const uint8_t*>(a.q + (static_cast<size_t>(sg.b) * a.R + r0) * kDqk);
+      const uint32_t total = static_cast<uint32_t>(rows) * kDqk * 2;
+      for (uint32_t off = 0; off < total; off += 16384) prefetch_l2(base + off, min(16384u, total - off));
+    };
+    {
+      SegIter look = it;
+      Seg first;
+      while (look.next(first))
+        if (!first.empty) {
+          prefetch_q(first);
+          break;
+        }
+    }
+    while (ok && it.next(s)) {
+      if (s.empty) continue;
+      {
+        SegIter look = it;
+        Seg nx;
+        while (look.next(nx))
+          if (!nx.empty) {
+            prefetch_q(nx);
             break;
           }
-          int pid = __ldg(bt + p);
-          int scale_pid = pid;
-          if (pid < 0 || pid >= a.num_pages) {
-            atomicOr(a.err, kErrBounds);
-            pid = a.num_pages;  // outside the tensor map: TMA fills zeros, no fault
-            scale_pid = 0;
+      }
+      const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
+      for (int p0 = s.page_lo; ok && p0 < s.page_hi; p0 += 32) {
+        const int my_p = p0 + lane;
+        const int my_pid = my_p < s.page_hi ? __ldg(bt + my_p) : 0;
+        const int cnt = min(32, s.page_hi - p0);
+        for (int k = 0; k < cnt; ++k) {
+          int pid = __shfl_sync(0xffffffffu, my_pid, k);
+          if (lane == 0) {
+            uint64_t* empty_bar = kFp8 ? &bars->f8_empty[stage] : &bars->kv_empty[stage];
+            uint64_t* full_bar = kFp8 ? &bars->f8_full[stage] : &bars->kv_full[stage];
+            if (!mbar_wait(smem_u32(empty_bar), ph ^ 1u, abort_flag)) {
+              ok = false;
+              if (!*abort_flag) signal_abort(bars, a.err, peer);
+            } else {
+              int scale_pid = pid;
+              if (pid < 0 || pid >= a.num_pages) {
+                atomicOr(a.err, kErrBounds);
+                pid = a.num_pages;  // outside the tensor map: TMA fills zeros, no fault
+                scale_pid = 0;
+              }
+              mbar_arrive_expect_tx(smem_u32(full_bar), bytes);
+              if (kFp8) {
+                uint8_t* dst = f8st + stage * C::kF8StageBytes;
+                for (int x = 0; x < nbox; ++x)
+                  tma_load_3d(smem_u32(dst + x * kBoxFp8), &kv_map, ch0 + 64 * x, 0, pid, smem_u32(full_bar));
+                bulk_load(smem_u32(dst + kMaxBoxes * kBoxFp8),
+                          a.kv_scales + static_cast<size_t>(scale_pid) * kPage * kGroups, kScaleBytes,
+                          smem_u32(full_bar));
+              } else {
+                uint8_t* dst = stages + stage * kStageBytes;
+                for (int x = 0; x < nbox; ++x)
+                  tma_load_3d(smem_u32(dst + x * kBoxBf16), &kv_map, ch0 + 64 * x, 0, pid, smem_u32(full_bar));
+              }
+              last_par[stage] = static_cast<int>(ph);
+            }
           }
-          mbar_arrive_expect_tx(smem_u32(full_bar), bytes);
-          if (kFp8) {
-            uint8_t* dst = f8st + stage * C::kF8StageBytes;
-            for (int x = 0; x < nbox; ++x)
-              tma_load_3d(smem_u32(dst + x * kBoxFp8), &kv_map, ch0 + 64 * x, 0, pid, smem_u32(full_bar));
-            bulk_load(smem_u32(dst + kMaxBoxes * kBoxFp8), a.kv_scales + static_cast<size_t>(scale_pid) * kPage * kGroups,
-                      kScaleBytes, smem_u32(full_bar));
-          } else {
-            uint8_t* dst = stages + stage * kStageBytes;
-            for (int x = 0; x < nbox; ++x)
-              tma_load_3d(smem_u32(dst + x * kBoxBf16), &kv_map, ch0 + 64 * x, 0, pid, smem_u32(full_bar));
-          }
-          last_par[stage] = static_cast<int>(ph);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
           if (++stage == (kFp8 ? C::kF8Stages : C::kStages)) {
             stage = 0;
             ph ^= 1u;
           }
         }
       }
-      if (!ok) {
-        // wait (time-bounded only) for the loads already in flight
-        for (int i = 0; i < (kFp8 ? C::kF8Stages : C::kStages); ++i)
-          if (last_par[i] >= 0)
-            mbar_wait(smem_u32(kFp8 ? &bars->f8_full[i] : &bars->kv_full[i]), (uint32_t)last_par[i], nullptr);
-      }
     }
+    if (!ok && lane == 0) {
+      // wait (time-bounded only) for the loads already in flight
+      for (int i = 0; i < (kFp8 ? C::kF8Stages : C::kStages); ++i)
+        if (last_par[i] >= 0)
+          mbar_wait(smem_u32(kFp8 ? &bars->f8_full[i] : &bars->kv_full[i]), (uint32_t)last_par[i], nullptr);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     SegIter it = it0;
@@ -301,48 +341,77 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       q_ph ^= 1u;
       const int n = s.page_hi - s.page_lo;
       int prev_stage = 0;
-      for (int j = 0; j <= n; ++j) {
-        if (j < n) {
-          if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
-          uint8_t* st = stages + stage * kStageBytes;
-          if (!kFp8) {
-            const int valid = seqlen - (s.page_lo + j) * kPage;
-            if (valid < kPage) zero_tail_rows(st, valid > 0 ? valid : 0, nbox, lane);
-            __syncwarp();
-          }
-          if (!mbar_wait(smem_u32(&bars->s_free), sfree_ph ^ 1u, abort_flag)) { ok = false; break; }
-          sfree_ph ^= 1u;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sbase = smem_u32(st);
-            for (int k = 0; k < nk; ++k) {
-              const uint64_t bd = smem_desc_sw128(sbase + (k >> 2) * kBoxBf16 + (k & 3) * 32, 16, 1024);
-              mma_ts(tbase + kColS, tbase + kColQ + 8 * k, bd, idesc_qk, k > 0 ? 1u : 0u);
+      // Step j issues QK(j) (j < n) and PV(j-1) (j > 0), whichever becomes
+      // ready first (QK first when both are): PV(j-1) never waits behind the
+      // arrival of page j.  Lane 0 probes the barriers without suspending and
+      // broadcasts, so the warp stays converged for the tail zeroing.
+      for (int j = 0; j <= n && ok; ++j) {
+        bool need_qk = j < n, need_pv = j > 0;
+        bool kv_ok = false, sf_ok = false, pf_ok = false, of_ok = (j != 1);
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t spins = 0;
+        auto probe = [&](uint64_t* bar, uint32_t parity) -> bool {
+          int r = 0;
+          if (lane == 0) r = mbar_test_wait(smem_u32(bar), parity) ? 1 : 0;
+          return __shfl_sync(0xffffffffu, r, 0) != 0;
+        };
+        while (need_qk || need_pv) {
+          bool did = false;
+          if (need_qk) {
+            if (!kv_ok) kv_ok = probe(&bars->kv_full[stage], ph);
+            if (kv_ok && !sf_ok) sf_ok = probe(&bars->s_free, sfree_ph ^ 1u);
+            if (kv_ok && sf_ok) {
+              sfree_ph ^= 1u;
+              uint8_t* st = stages + stage * kStageBytes;
+              if (!kFp8) {
+                const int valid = seqlen - (s.page_lo + j) * kPage;
+                if (valid < kPage) zero_tail_rows(st, valid > 0 ? valid : 0, nbox, lane);
+                __syncwarp();
+              }
+              tc_fence_after();
+              if (lane == 0) {
+                const uint32_t sbase = smem_u32(st);
+                for (int k = 0; k < nk; ++k) {
+                  const uint64_t bd = smem_desc_sw128(sbase + (k >> 2) * kBoxBf16 + (k & 3) * 32, 16, 1024);
+                  mma_ts(tbase + kColS, tbase + kColQ + 8 * k, bd, idesc_qk, k > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars->s_full));
+              }
+              __syncwarp();
+              need_qk = false;
+              did = true;
             }
-            mma_commit(smem_u32(&bars->s_full));
           }
-          __syncwarp();
-        }
-        if (j > 0) {
-          if (!mbar_wait(smem_u32(&bars->p_full), pfull_ph, abort_flag)) { ok = false; break; }
-          pfull_ph ^= 1u;
-          if (j == 1) {
-            if (!mbar_wait(smem_u32(&bars->o_free), ofree_ph ^ 1u, abort_flag)) { ok = false; break; }
-            ofree_ph ^= 1u;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t vbase = smem_u32(stages + prev_stage * kStageBytes);
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t bd = smem_desc_sw128(vbase + k * 2048, 8192, 1024);
-              mma_ts(tbase + kColO, tbase + kColP + 8 * k, bd, idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+          if (need_pv) {
+            if (!pf_ok) pf_ok = probe(&bars->p_full, pfull_ph);
+            if (pf_ok && !of_ok) of_ok = probe(&bars->o_free, ofree_ph ^ 1u);
+            if (pf_ok && of_ok) {
+              pfull_ph ^= 1u;
+              if (j == 1) ofree_ph ^= 1u;
+              tc_fence_after();
+              if (lane == 0) {
+                const uint32_t vbase = smem_u32(stages + prev_stage * kStageBytes);
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t bd = smem_desc_sw128(vbase + k * 2048, 8192, 1024);
+                  mma_ts(tbase + kColO, tbase + kColP + 8 * k, bd, idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars->p_free));
+                mma_commit(smem_u32(&bars->kv_empty[prev_stage]));
+                if (j == n) mma_commit(smem_u32(&bars->o_full));
+              }
+              __syncwarp();
+              need_pv = false;
+              did = true;
             }
-            mma_commit(smem_u32(&bars->p_free));
-            mma_commit(smem_u32(&bars->kv_empty[prev_stage]));
-            if (j == n) mma_commit(smem_u32(&bars->o_full));
           }
-          __syncwarp();
+          if (!did && ((++spins & 15u) == 0u)) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitNs) {
+              ok = false;
+              break;
+            }
+          }
         }
+        if (!ok) break;
         if (j < n) {
           prev_stage = stage;
           if (++stage == C::kStages) {
@@ -398,23 +467,31 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         qmul = ldexpf(1.f, k);
       }
       const uint4* src = row + ch0 / 8;
-      for (int cc = 0; cc < nbox; ++cc) {
-        uint32_t w[32];
+      for (int c2 = 0; c2 < nbox; c2 += 2) {  // two 64-channel chunks of loads in flight
+        uint4 x[16];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          uint4 x = valid ? __ldg(src + cc * 8 + v) : make_uint4(0, 0, 0, 0);
-          if (kFp8) {
-            x.x = pack_f16x2(bf16_lo(x.x) * qs, bf16_hi(x.x) * qs);
-            x.y = pack_f16x2(bf16_lo(x.y) * qs, bf16_hi(x.y) * qs);
-            x.z = pack_f16x2(bf16_lo(x.z) * qs, bf16_hi(x.z) * qs);
-            x.w = pack_f16x2(bf16_lo(x.w) * qs, bf16_hi(x.w) * qs);
+        for (int v = 0; v < 16; ++v)
+          x[v] = (valid && (c2 + (v >> 3)) < nbox) ? __ldg(src + c2 * 8 + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (c2 + h >= nbox) break;
+          uint32_t w[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint4 y = x[8 * h + v];
+            if (kFp8) {
+              y.x = pack_f16x2(bf16_lo(y.x) * qs, bf16_hi(y.x) * qs);
+              y.y = pack_f16x2(bf16_lo(y.y) * qs, bf16_hi(y.y) * qs);
+              y.z = pack_f16x2(bf16_lo(y.z) * qs, bf16_hi(y.z) * qs);
+              y.w = pack_f16x2(bf16_lo(y.w) * qs, bf16_hi(y.w) * qs);
+            }
+            w[4 * v + 0] = y.x;
+            w[4 * v + 1] = y.y;
+            w[4 * v + 2] = y.z;
+            w[4 * v + 3] = y.w;
           }
-          w[4 * v + 0] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
+          tmem_st32(tbase + lane_off + kColQ + 32 * (c2 + h), w);
         }
-        tmem_st32(tbase + lane_off + kColQ + 32 * cc, w);
       }
       tmem_wait_st();
       tc_fence_before();

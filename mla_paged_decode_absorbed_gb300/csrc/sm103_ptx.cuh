@@ -80,6 +80,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of a phase (never suspends the thread), for polling
+// several barriers from one thread.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Same as mbar_try_wait but with acquire semantics at cluster scope, for
 // barriers whose phase is completed by writes from the peer CTA.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -167,6 +181,12 @@ __device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* gsrc, u
           smem_dst),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Bulk prefetch of global memory into L2 (address and size 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+               : "memory");
 }
 
 // ------------------------------------------------------------------- tcgen05
