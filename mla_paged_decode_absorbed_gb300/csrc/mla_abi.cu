@@ -340,6 +340,7 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   if (st != MLA_OK) return st;
   DecodeArgs a;
   a.q = static_cast<const uint16_t*>(q);
+  a.kv = kv;
   a.kv_scales = kv_scales;
   a.block_table = bt;
   a.seqlens = seqlens;

@@ -21,6 +21,7 @@ enum : int { kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters 
 
 struct DecodeArgs {
   const uint16_t* q;          // bf16 [B, s_q, H, 576]
+  const void* kv;             // the cache itself (the fp8 variant reads it with plain loads)
   const float* kv_scales;     // fp32 [P, 64, 5] (fp8 cache) or nullptr
   const int32_t* block_table; // [B, max_pages]
   const int32_t* seqlens;     // [B]

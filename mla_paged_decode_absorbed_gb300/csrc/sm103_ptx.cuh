@@ -149,6 +149,21 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float
       : "memory");
 }
 
+__device__ __forceinline__ void st_async_v4_u32(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          remote_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr),
+               "f"(v), "r"(remote_bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_u32(uint32_t remote_addr, uint32_t v) {
   asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(remote_addr), "r"(v) : "memory");
 }
