@@ -81,7 +81,7 @@ typedef struct {
 /*
  * Bytes of device workspace mla_decode() needs for `desc` on a device with
  * `num_sms` SMs (num_sms <= 0: query the current device).  The workspace holds
- * the error word, the split plan and the fp32 partial outputs of split
+ * the error word, the split plan and the partial outputs of split
  * requests.  Returns 0 for an invalid desc.
  */
 size_t mla_workspace_size(const mla_desc* desc, int num_sms);
@@ -127,9 +127,17 @@ mla_status mla_plan(const mla_desc* desc, const int32_t* seqlens, void* workspac
 
 /*
  * Step 2 (attention over the pages, one kernel of 2-CTA clusters): needs the
- * plan of mla_plan() in the same workspace.  Writes out/lse for requests that
- * were not split, and fp32 partials (normalised output + lse per piece) in the
- * workspace for requests that were.  Arguments as for mla_decode().
+ * plan of mla_plan() in the same workspace.  Writes out/lse for units that
+ * were not split.  Every piece of a split unit writes a partial (normalised
+ * output in fp16 with a power-of-two row scale, and its lse) into the
+ * workspace; for a unit of at most four pieces the piece that finishes last
+ * merges the others' partials with its own result and writes out/lse itself.
+ * Units of more pieces are left to mla_combine().  The kernel leaves the
+ * workspace's merge counters clear, so it may run again on the same plan;
+ * after a device error, run mla_plan() again first.  The kernel is launched
+ * as a programmatic dependent of the previous kernel in `stream` (its prologue
+ * may overlap it; it reads nothing before that kernel has finished).
+ * Arguments as for mla_decode().
  */
 mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void* kv_pages,
                                 const float* kv_scales, const int32_t* block_table, const int32_t* seqlens,
@@ -137,10 +145,12 @@ mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void*
                                 size_t workspace_bytes, void* stream);
 
 /*
- * Step 3 (LSE-weighted combine, one kernel): for every split request,
+ * Step 3 (LSE-weighted combine, one kernel): for every split unit of more
+ * than four pieces,
  *   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
  * over its pieces, written to out (bf16) and lse.  Needs the plan and the
- * partials of the two previous steps in the same workspace.
+ * partials of the two previous steps in the same workspace; returns at once
+ * on the device when the plan has no such unit.
  */
 mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* workspace, size_t workspace_bytes,
                        void* stream);
@@ -166,7 +176,7 @@ mla_status mla_get_device_error(const void* workspace, void* stream);
  * The first call on a device looks up the array's device address (make it
  * before any stream capture).  The call uses at most 76 two-CTA clusters; a
  * problem whose plan and partials need more than 40 MiB (more than about
- * 500,000 (row block, request) units) returns MLA_ERR_WORKSPACE and launches
+ * 5,000,000 (row block, request) units) returns MLA_ERR_WORKSPACE and launches
  * nothing.
  * All calls share the array: calls that overlap on the GPU race, so serialise
  * them.  With check_device_error != 0 the call synchronises `stream` and
@@ -182,11 +192,17 @@ const char* mla_status_string(int status);
 
 /* Byte offsets of the workspace regions (for tests and tools that inspect the
  * plan).  The header is int32 words: [0] error bits, [1] W, [2] total cost,
- * [3] units, [4] clusters, [5] plan overhead.  cl_first is int32 [clusters]
- * (first unit each cluster touches), pre is int32 [units + 1] (cost prefix),
- * lse_part fp32 [2*clusters, 128], o_part fp32 [2*clusters, 128, 512]. */
+ * [3] units, [4] clusters, [5] plan overhead, [6] 1 if some unit has more than
+ * four pieces (mla_combine() has work).  cl_first is int32 [clusters] (first
+ * unit each cluster touches), pre is int32 [units + 1] (cost prefix), sync is
+ * int32 [3*clusters] (merge counters, then partial-slot ready flags; mla_plan()
+ * clears them and every completed attention kernel leaves them clear),
+ * lse_part fp32 [2*clusters, 128, 2] (lse of the piece, power-of-two scale of
+ * its stored output), o_part fp16 [2*clusters][64 chunks][128 rows][8] (slot
+ * s, row r, channel ch at ((s*64 + ch/8)*128 + r)*8 + ch%8; the piece's
+ * normalised output is the stored value times the scale). */
 typedef struct {
-  size_t header, cl_first, pre, lse_part, o_part, total;
+  size_t header, cl_first, pre, lse_part, o_part, sync, total;
 } mla_workspace_layout;
 mla_status mla_get_workspace_layout(const mla_desc* desc, int num_clusters, mla_workspace_layout* layout);
 

@@ -56,7 +56,7 @@ class MlaDesc(ctypes.Structure):
 
 
 class MlaWorkspaceLayout(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "cl_first", "pre", "lse_part", "o_part", "total")]
+    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "cl_first", "pre", "lse_part", "o_part", "sync", "total")]
 
 
 class MlaError(RuntimeError):

@@ -3,6 +3,7 @@
 // kernel, tensor-map encoding and the launch sequence on the caller's stream.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -18,8 +19,8 @@ namespace mla_gb300 {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kCombineRowsPerCta = 2;
-constexpr int kCombineThreads = 256;
+constexpr int kCombineChunksPerCta = 2;  // 8-channel chunks of every row per combine CTA
+constexpr int kCombineThreads = 128 * kCombineChunksPerCta;
 
 // ------------------------------------------------------------------ planner
 // Cost of unit u (row block rb = u / B of request b = u % B): the pages the
@@ -40,15 +41,25 @@ __device__ __forceinline__ int unit_cost(const int32_t* seqlens, int u, int B, i
 }
 
 // One CTA: per-unit costs, their exclusive prefix sum `pre`, the per-cluster
-// budget W = ceil(total / G), and the first unit each cluster touches.
+// budget W = ceil(total / G), the first unit each cluster touches, and whether
+// some unit has more than kFuseMax pieces.  Also clears the merge counters and
+// partial-slot flags the attention kernel uses.
 __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* seqlens, int B, int s_q, int H,
                                                                 int R, int U, int max_pages, int G, int ovh,
-                                                                int32_t* hdr, int32_t* cl_first, int32_t* pre) {
+                                                                int32_t* hdr, int32_t* cl_first, int32_t* pre,
+                                                                int32_t* sync) {
   __shared__ int warp_sum[32];
   __shared__ int s_W;
+  // the attention kernel may start its prologue now; it reads the plan only
+  // after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" :::);
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) hdr[kHdrErr] = 0;
+  if (tid == 0) {
+    hdr[kHdrErr] = 0;
+    hdr[kHdrCombine] = 0;
+  }
+  for (int i = tid; i < 3 * G; i += T) sync[i] = 0;
   __syncthreads();
   int32_t* err = hdr + kHdrErr;
   const int chunk = (U + T - 1) / T;
@@ -97,18 +108,29 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
   for (int c = tid; c < G; c += T) cl_first[c] = U;
   __syncthreads();
   const int W = s_W;
+  bool many = false;
   for (int u = u0; u < u1; ++u) {
     const int p0 = pre[u], p1 = pre[u + 1];
     const int cf = (p0 + W - 1) / W, cl = (p1 + W - 1) / W - 1;
     for (int c = cf; c <= cl && c < G; ++c) cl_first[c] = u;
+    if (p1 - p0 > ovh && (p1 - 1) / W - (p0 + ovh) / W + 1 > kFuseMax) many = true;
   }
+  if (many) atomicOr(hdr + kHdrCombine, 1);
 }
 
 // ------------------------------------------------------------------ combine
-// CTA (c, y): the unit whose pages start in cluster c's range and continue
-// past it (at most one per cluster) is merged here, rows [2y, 2y+2) of it:
-//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k.
+// Units with at most kFuseMax pieces are merged inside the attention kernel;
+// this kernel merges the others.  CTA (c, y): the unit whose pages start in
+// cluster c's range and continue past it (at most one per cluster), 8-channel
+// chunks [2y, 2y + 2) of every row (one row per thread, so the chunk-
+// interleaved fp16 partial slots are read with coalesced loads):
+//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
+// where out_k = stored_k * scale_k.  Two passes over the pieces (lse max,
+// then the weighted sum), so all loads of a pass are independent.
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
+  // launched as a programmatic dependent of the attention kernel: wait for it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.hdr[kHdrCombine] == 0) return;  // nothing to do: every split unit was merged in place
   const int c = blockIdx.x;
   if (c + 1 >= a.clusters) return;
   const int W = a.hdr[kHdrW];
@@ -120,49 +142,48 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const int lo_c = c * W, hi_c = lo_c + W;
   if (!(first >= lo_c && first < hi_c && p1 > hi_c)) return;
   const int last = (p1 - 1) / W;
+  if (last - c + 1 <= kFuseMax) return;
   const int b = u % a.B, rb = u / a.B;
-  const int L = blockIdx.y * kCombineRowsPerCta + (threadIdx.x >> 7);  // one row per 128 threads
-  const int t = threadIdx.x & 127;                                      // four channels per thread
+  const int L = threadIdx.x & (kRowsPerBlock - 1);                      // row within the block
+  const int j = blockIdx.y * kCombineChunksPerCta + (threadIdx.x >> 7);  // 8-channel chunk
   const int r = rb * kRowsPerBlock + L;
   if (r >= a.R) return;
-  // one pass over the pieces with a running max (pieces are independent, so
-  // their loads overlap); rows no piece saw keep lse = -inf and a zero output
-  float mx = -INFINITY, wsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int cc = c; cc <= last; ++cc) {
-    const int slot = (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc;
-    const float lk = a.lse_part[static_cast<size_t>(slot) * kRowsPerBlock + L];
-    const float4 o =
-        reinterpret_cast<const float4*>(a.o_part + (static_cast<size_t>(slot) * kRowsPerBlock + L) * kDv)[t];
-    if (lk == -INFINITY) continue;
-    const float m_new = fmaxf(mx, lk);
-    const float scale_old = expf(mx - m_new);  // 0 when mx is -inf
-    const float w = expf(lk - m_new);
-    acc.x = acc.x * scale_old + w * o.x;
-    acc.y = acc.y * scale_old + w * o.y;
-    acc.z = acc.z * scale_old + w * o.z;
-    acc.w = acc.w * scale_old + w * o.w;
-    wsum = wsum * scale_old + w;
-    mx = m_new;
+  const float2* lp = reinterpret_cast<const float2*>(a.lse_part);
+  const uint4* op = reinterpret_cast<const uint4*>(a.o_part);
+  auto slot_of = [&](int cc) { return (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc; };
+  float mx = -INFINITY;
+#pragma unroll 8
+  for (int cc = c; cc <= last; ++cc) mx = fmaxf(mx, lp[static_cast<size_t>(slot_of(cc)) * kRowsPerBlock + L].x);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll 8
+    for (int cc = c; cc <= last; ++cc) {
+      const int slot = slot_of(cc);
+      const float2 ls = lp[static_cast<size_t>(slot) * kRowsPerBlock + L];
+      const uint4 o = op[(static_cast<size_t>(slot) * kPartChunks + j) * kRowsPerBlock + L];
+      const float w = expf(ls.x - mx);  // 0 for a piece that saw no key of this row
+      wsum += w;
+      const float ws = w * ls.y;
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ow[h]));
+        acc[2 * h] += ws * f.x;
+        acc[2 * h + 1] += ws * f.y;
+      }
+    }
   }
-  float lse_v = -INFINITY;
-  if (wsum > 0.f) {
-    const float inv = 1.f / wsum;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
-    lse_v = mx + logf(wsum);
-  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const size_t orow = static_cast<size_t>(b) * a.R + r;
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 packed;
-  packed.x = *reinterpret_cast<uint32_t*>(&lo);
-  packed.y = *reinterpret_cast<uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(a.out + orow * kDv)[t] = packed;
-  if (t == 0) a.lse[orow] = lse_v;
+  uint32_t packed[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * h] * inv, acc[2 * h + 1] * inv);
+    packed[h] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  reinterpret_cast<uint4*>(a.out + orow * kDv)[j] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  if (j == 0) a.lse[orow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host helpers
@@ -210,10 +231,12 @@ mla_workspace_layout layout_for(const Dims& x, int G) {
   off += align256(sizeof(int32_t) * static_cast<size_t>(G));
   l.pre = off;
   off += align256(sizeof(int32_t) * (static_cast<size_t>(x.U) + 1));
+  l.sync = off;
+  off += align256(sizeof(int32_t) * 3 * static_cast<size_t>(G));
   l.lse_part = off;
-  off += align256(sizeof(float) * 2 * static_cast<size_t>(G) * kRowsPerBlock);
+  off += align256(sizeof(float) * 2 * 2 * static_cast<size_t>(G) * kRowsPerBlock);
   l.o_part = off;
-  off += sizeof(float) * 2 * static_cast<size_t>(G) * kRowsPerBlock * kDv;
+  off += sizeof(uint16_t) * 2 * static_cast<size_t>(G) * kRowsPerBlock * kDv;
   l.total = align256(off);
   return l;
 }
@@ -267,23 +290,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [num_pages, 64, 576] cache viewed as a 3-D tensor; one box = 64 channels x 64
-// tokens of one page.  bf16 boxes are 128-byte rows with the 128-byte swizzle
-// the MMA descriptors expect; e4m3 boxes are plain 64-byte rows.
-mla_status make_kv_map(const void* kv, int num_pages, bool fp8, CUtensorMap* map) {
+// The bf16 [num_pages, 64, 576] cache as a 4-D tensor (64 channels, 64
+// tokens, 9 channel chunks, pages) whose chunk stride is 128 bytes: one box of
+// 64 x 64 x `chunks` x 1 brings channel blocks 0..chunks-1 of a page in a
+// single copy, laid out in shared memory as consecutive 64-token x 64-channel
+// blocks with the 128-byte swizzle the MMA descriptors expect.
+mla_status make_kv_map4(const void* kv, int num_pages, int chunks, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return MLA_ERR_CUDA;
-  const cuuint64_t esz = fp8 ? 1 : 2;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(kPage),
-                        static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[2] = {kDqk * esz, kDqk * esz * kPage};
-  cuuint32_t box[3] = {64, 64, 1};
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(kPage), 9, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {kDqk * 2, 128, kDqk * 2 * kPage};
+  cuuint32_t box[4] = {64, 64, static_cast<cuuint32_t>(chunks), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
   std::memset(map, 0, sizeof(*map));
-  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                   const_cast<void*>(kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
@@ -328,16 +350,23 @@ mla_status run_plan(const Prepared& p, const int32_t* seqlens, cudaStream_t stre
   int32_t* hdr = reinterpret_cast<int32_t*>(p.ws + p.lay.header);
   mla_plan_kernel<<<1, kPlanThreads, 0, stream>>>(seqlens, p.x.B, p.x.s_q, p.x.H, p.x.R, p.x.U, p.x.maxp, p.G,
                                                   p.x.ovh, hdr, reinterpret_cast<int32_t*>(p.ws + p.lay.cl_first),
-                                                  reinterpret_cast<int32_t*>(p.ws + p.lay.pre));
+                                                  reinterpret_cast<int32_t*>(p.ws + p.lay.pre),
+                                                  reinterpret_cast<int32_t*>(p.ws + p.lay.sync));
   return launch_status(cudaGetLastError());
 }
 
 mla_status run_attention(const Prepared& p, const void* q, const void* kv, const float* kv_scales,
                          const int32_t* bt, const int32_t* seqlens, float scale, void* out, float* lse,
                          cudaStream_t stream) {
-  CUtensorMap map;
-  mla_status st = make_kv_map(kv, p.x.P, p.x.fp8, &map);
-  if (st != MLA_OK) return st;
+  // the fp8 variant reads pages with plain loads and uses neither map
+  CUtensorMap map9, map8;
+  std::memset(&map9, 0, sizeof(map9));
+  std::memset(&map8, 0, sizeof(map8));
+  if (!p.x.fp8) {
+    mla_status st = make_kv_map4(kv, p.x.P, 9, &map9);
+    if (st == MLA_OK) st = make_kv_map4(kv, p.x.P, 8, &map8);
+    if (st != MLA_OK) return st;
+  }
   DecodeArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.kv = kv;
@@ -349,8 +378,10 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   a.pre = reinterpret_cast<const int32_t*>(p.ws + p.lay.pre);
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
-  a.o_part = reinterpret_cast<float*>(p.ws + p.lay.o_part);
+  a.o_part = p.ws + p.lay.o_part;
   a.lse_part = reinterpret_cast<float*>(p.ws + p.lay.lse_part);
+  a.unit_cnt = reinterpret_cast<int32_t*>(p.ws + p.lay.sync);
+  a.slot_ready = a.unit_cnt + p.G;
   a.err = reinterpret_cast<int32_t*>(p.ws + p.lay.header);
   a.B = p.x.B;
   a.s_q = p.x.s_q;
@@ -362,7 +393,7 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   a.max_pages = p.x.maxp;
   a.overhead = p.x.ovh;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(launch_decode(a, map, p.G, p.x.fp8, stream));
+  return launch_status(launch_decode(a, map9, map8, p.G, p.x.fp8, stream));
 }
 
 mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t stream) {
@@ -370,7 +401,7 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   a.hdr = reinterpret_cast<const int32_t*>(p.ws + p.lay.header);
   a.cl_first = reinterpret_cast<const int32_t*>(p.ws + p.lay.cl_first);
   a.pre = reinterpret_cast<const int32_t*>(p.ws + p.lay.pre);
-  a.o_part = reinterpret_cast<const float*>(p.ws + p.lay.o_part);
+  a.o_part = p.ws + p.lay.o_part;
   a.lse_part = reinterpret_cast<const float*>(p.ws + p.lay.lse_part);
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
@@ -379,9 +410,17 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   a.U = p.x.U;
   a.clusters = p.G;
   a.overhead = p.x.ovh;
-  dim3 grid(p.G, kRowsPerBlock / kCombineRowsPerCta);
-  mla_combine_kernel<<<grid, kCombineThreads, 0, stream>>>(a);
-  return launch_status(cudaGetLastError());
+  // programmatic dependent of the attention kernel (it waits on the device)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G, kPartChunks / kCombineChunksPerCta, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launch_status(cudaLaunchKernelEx(&cfg, mla_combine_kernel, a));
 }
 
 }  // namespace

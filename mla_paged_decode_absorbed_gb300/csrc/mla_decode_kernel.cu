@@ -57,13 +57,19 @@ constexpr int kStageS = 9 * kBox;                  // scorer: channels 0..575
 constexpr int kStageO = 8 * kBox;                  // accumulator: channels 0..511
 constexpr int kPBytes = kRowsPerBlock * 64 * 2;    // P tile: 128 rows x 64 keys, SW128 K-major
 constexpr int kVecBytes = kRowsPerBlock * 4;       // one fp32 per row
+constexpr int kPartBytes = kPartChunks * kRowsPerBlock * 16;  // one fp16 partial slot (128 KB)
+static_assert(kPartBytes <= kStages * kStageO, "a partial slot must fit in the page ring");
 
 // Shared-memory layout (byte offsets from the 1024-aligned base; the same in
-// both CTAs, each uses its part).
+// both CTAs, each uses its part).  Both CTAs keep their page ring at offset 0.
+constexpr int kQStageBytes = 32 * 64;              // scorer: per softmax warp, 32 rows x 32 channels
+constexpr int kOffQStage = kStages * kStageS;      // scorer: Q transpose staging [4]
+constexpr int kScorerEnd = kOffQStage + 4 * kQStageBytes;
 constexpr int kOffP = kStages * kStageO;           // accumulator: P tiles [2]
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;     // accumulator: rescale factors [2][128]
-constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: row sums [2][128]
-constexpr int kOffBars = (kStages * kStageS > kOffL + 2 * kVecBytes) ? kStages * kStageS : kOffL + 2 * kVecBytes;
+constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: (row sum, lse) [128]
+constexpr int kAccEnd = kOffL + kRowsPerBlock * 8;
+constexpr int kOffBars = kScorerEnd > kAccEnd ? kScorerEnd : kAccEnd;
 constexpr int kBarBytes = 256;
 constexpr int kSmemMax = 232448;
 constexpr int kSmem = kSmemMax;                    // layout + slack for aligning the base
@@ -75,6 +81,7 @@ constexpr uint32_t kColQ = 0, kColS0 = 288, kColS1 = 352;
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool kFp8>
 struct Cfg {
@@ -88,7 +95,7 @@ struct Bars {
   uint64_t s_full[2];     // scorer: QK done (commit)
   uint64_t s_free[2];     // scorer: S read by the softmax (128)
   uint64_t pbuf_free[2];  // scorer: accumulator finished with P tile b (remote, 1)
-  uint64_t l_free[2];     // scorer: accumulator read row sums b (remote, 4)
+  uint64_t l_free;        // scorer: accumulator read the row sums (remote, 4)
   uint64_t p_full[2];     // accumulator: P tile + factors arrived (1 + tx)
   uint64_t corr_done[2];  // accumulator: O rescaled if needed for tile parity b (128).  Two
                           // of them: the rescale warps may finish tile t+1 before the MMA
@@ -96,10 +103,14 @@ struct Bars {
   uint64_t pv_done[2];    // accumulator: PV of tile with parity b done (commit)
   uint64_t o_full;        // accumulator: last PV of a segment done (commit)
   uint64_t o_free;        // accumulator: epilogue read O (128)
-  uint64_t l_full[2];     // accumulator: row sums arrived (1 + tx)
+  uint64_t l_full;        // accumulator: row sums + lse arrived (1 + tx)
+  uint64_t mrg_bar;       // accumulator: a partial of another piece arrived in the ring (1 + tx)
+  uint64_t epi_bar;       // accumulator: barrier of the four epilogue warps (128), bounded
+                          // unlike bar.sync, so a warp that gives up cannot strand the others
   uint64_t drain;
   int abort_flag;
   uint32_t tmem_base;
+  int ticket;             // accumulator: finish order of this piece among its unit's pieces
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block too large");
 
@@ -174,6 +185,35 @@ __device__ __forceinline__ void zero_tail_rows(uint8_t* stage, int valid, int nb
   fence_proxy_async_smem();
 }
 
+// Writes output channels [64*cc, 64*cc + 64) of a warp's 32 rows: thread
+// `lane` holds row `lane` (64 final values).  The rows are staged through
+// `est` (4 KB, 16-byte chunks XOR-swizzled by row) so that each store
+// instruction writes four whole 128-byte lines (8 lanes per row) instead of
+// 32 scattered pieces.  Rows at or past `rows_left` are not written.
+__device__ __forceinline__ void store_rows_bf16(uint8_t* est, const float (&v)[64], uint16_t* dst, int rows_left,
+                                                int cc, int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(est + lane * 128 + ((q ^ (lane & 7)) << 4)) = w;
+  }
+  __syncwarp();
+  const int rsub = lane >> 3, csub = lane & 7;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int rr = 4 * k + rsub;
+    if (rr < rows_left) {
+      const uint4 y = *reinterpret_cast<const uint4*>(est + rr * 128 + ((csub ^ (rr & 7)) << 4));
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(rr) * kDv + 64 * cc + 8 * csub) = y;
+    }
+  }
+  __syncwarp();
+}
+
 // e4m3 x2 -> two floats (exact through f16).
 __device__ __forceinline__ void e4m3x2_to_f32(uint16_t v, float& lo, float& hi) {
   uint32_t h2;
@@ -195,7 +235,8 @@ __device__ __forceinline__ float max64(const float (&x)[64]) {
 
 template <bool kFp8>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map9, const __grid_constant__ CUtensorMap kv_map8,
+                      const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -206,6 +247,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const bool scorer = rank == 0;
   if (pad > static_cast<uint32_t>(kAlignSlack)) {  // never expected: report, do nothing
+    griddep_wait();  // the planner clears the error word first
     if (tid == 0) atomicOr(a.err, kErrTimeout);
     return;
   }
@@ -220,20 +262,22 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(smem_u32(&bars->s_full[i]), 1);
       mbar_init(smem_u32(&bars->s_free[i]), 128);
       mbar_init(smem_u32(&bars->pbuf_free[i]), 1);
-      mbar_init(smem_u32(&bars->l_free[i]), 4);
       mbar_init(smem_u32(&bars->p_full[i]), 1);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
-      mbar_init(smem_u32(&bars->l_full[i]), 1);
     }
     mbar_init(smem_u32(&bars->corr_done[0]), 128);
     mbar_init(smem_u32(&bars->corr_done[1]), 128);
     mbar_init(smem_u32(&bars->o_full), 1);
     mbar_init(smem_u32(&bars->o_free), 128);
+    mbar_init(smem_u32(&bars->l_free), 4);
+    mbar_init(smem_u32(&bars->l_full), 1);
+    mbar_init(smem_u32(&bars->mrg_bar), 1);
+    mbar_init(smem_u32(&bars->epi_bar), 128);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
-  if (warp == 0 && lane == 0 && !kFp8) tma_prefetch_desc(&kv_map);
+  if (warp == 0 && lane == 0 && !kFp8) tma_prefetch_desc(scorer ? &kv_map9 : &kv_map8);
   if (warp == 1) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
@@ -242,6 +286,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   __syncthreads();
   cluster_sync_all();
   tc_fence_after();
+  // Everything above overlaps the planner kernel (programmatic dependent
+  // launch); the plan, the error word and the outputs are touched only after
+  // the planner has finished.
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tbase = bars->tmem_base;
   const volatile int* abort_flag = &bars->abort_flag;
 
@@ -263,27 +312,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- loader
     // The whole warp walks the segments; lane 0 waits and issues the copies.
-    // Page ids are read 32 at a time (one per lane) and shuffled out.
+    // Page ids are read 32 at a time (one per lane) and shuffled out.  Each
+    // page is ONE 4-D copy (the TMA unit spends a fixed time per copy, so few
+    // large copies keep it fastest); the accumulator's read of a page is its
+    // last use (the scorer read it a little earlier), so it is marked to be
+    // evicted from L2 first.  Nothing else is issued to the TMA unit here.
     SegIter it = it0;
     Seg s;
-    // L2 prefetch of a segment's Q rows (contiguous), one segment ahead.
-    auto prefetch_q = [&](const Seg& sg) {
-      if (!scorer || lane != 0 || sg.empty) return;
-      const int r0 = sg.rb * kRowsPerBlock;
-      const int rows = min(kRowsPerBlock, a.R - r0);
-      const uint8_t* base = reinterpret_cast<const uint8_t*>(a.q + (static_cast<size_t>(sg.b) * a.R + r0) * kDqk);
-      const uint32_t total = static_cast<uint32_t>(rows) * kDqk * 2;
-      for (uint32_t off = 0; off < total; off += 16384) prefetch_l2(base + off, min(16384u, total - off));
-    };
-    {
-      SegIter look = it;
-      Seg first;
-      while (look.next(first))
-        if (!first.empty) {
-          prefetch_q(first);
-          break;
-        }
-    }
+    const uint64_t policy = l2_policy_evict_first();
     int stage = 0;
     uint32_t ph = 0;
     int last_par[kStages];
@@ -292,15 +328,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t bytes = static_cast<uint32_t>(nbox * kBox);
     while (ok && it.next(s)) {
       if (s.empty) continue;
-      {
-        SegIter look = it;
-        Seg nx;
-        while (look.next(nx))
-          if (!nx.empty) {
-            prefetch_q(nx);
-            break;
-          }
-      }
       if (kFp8) continue;  // the fp8 variant's dequant warps read pages themselves
       const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
       for (int p0 = s.page_lo; ok && p0 < s.page_hi; p0 += 32) {
@@ -321,7 +348,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               const uint32_t fb = smem_u32(&bars->kv_full[stage]);
               mbar_arrive_expect_tx(fb, bytes);
               uint8_t* dst = smem + stage * stage_bytes;
-              for (int x = 0; x < nbox; ++x) tma_load_3d(smem_u32(dst + x * kBox), &kv_map, 64 * x, 0, pid, fb);
+              if (scorer)
+                tma_load_4d(smem_u32(dst), &kv_map9, 0, 0, 0, pid, fb);
+              else
+                tma_load_4d_hint(smem_u32(dst), &kv_map8, 0, 0, 0, pid, fb, policy);
               last_par[stage] = static_cast<int>(ph);
             }
           }
@@ -442,58 +472,101 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const uint32_t rL = mapa_shared(smem_u32(smem + kOffL), peer);
       const uint32_t rPfull0 = mapa_shared(smem_u32(&bars->p_full[0]), peer);
       const uint32_t rPfull1 = mapa_shared(smem_u32(&bars->p_full[1]), peer);
-      const uint32_t rLfull0 = mapa_shared(smem_u32(&bars->l_full[0]), peer);
-      const uint32_t rLfull1 = mapa_shared(smem_u32(&bars->l_full[1]), peer);
+      const uint32_t rLfull = mapa_shared(smem_u32(&bars->l_full), peer);
       uint32_t q_loaded = 0;
       float qmul = 1.f, qmul_next = 1.f;
 
-      // Q row of this thread -> TMEM (all 576 channels, A operand of QK).  The
-      // fp8-cache variant computes in fp16: the row is scaled by a power of
-      // two so |q| <= 16384 (no overflow), undone on the scores.
+      // Q rows of this warp (its TMEM lane quarter) -> TMEM, all 576 channels
+      // (the A operand of QK).  The loads are coalesced: per 32-channel step
+      // a warp instruction reads 8 rows x 64 contiguous bytes, and the step
+      // is transposed through a 2 KB shared staging area so that each thread
+      // then holds its own row for tcgen05.st.  The fp8-cache variant computes
+      // in fp16: the row is scaled by a power of two so |q| <= 16384 (no
+      // overflow), undone on the scores.
+      uint8_t* const qst = smem + kOffQStage + wq * kQStageBytes;
       auto load_q = [&](const Seg& sg) -> float {
-        const int r = sg.rb * kRowsPerBlock + L;
-        const bool valid = r < a.R;
-        const uint4* row =
-            reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(sg.b) * a.R + (valid ? r : 0)) * kDqk);
+        const int r0 = sg.rb * kRowsPerBlock + wq * 32;  // first row of this warp
+        const int rsub = lane >> 2, csub = lane & 3;     // load view: rows rsub + 8i, 16-byte chunk csub
+        const uint8_t* qb = reinterpret_cast<const uint8_t*>(a.q) + static_cast<size_t>(sg.b) * a.R * (kDqk * 2);
+        bool rv[4];
+        const uint8_t* rp[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + rsub + 8 * i;
+          rv[i] = r < a.R;
+          rp[i] = qb + static_cast<size_t>(rv[i] ? r : 0) * (kDqk * 2) + csub * 16;
+        }
         float qs = 1.f, qm = 1.f;
-        if (kFp8 && valid) {
-          float amax = 0.f;
-          for (int v = 0; v < kDqk / 8; ++v) {
-            const uint4 x = __ldg(row + v);
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(x.x)), fabsf(bf16_hi(x.x))),
-                                     fmaxf(fabsf(bf16_lo(x.y)), fabsf(bf16_hi(x.y)))));
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(x.z)), fabsf(bf16_hi(x.z))),
-                                     fmaxf(fabsf(bf16_lo(x.w)), fabsf(bf16_hi(x.w)))));
+        if (kFp8) {
+          float am[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int s0 = 0; s0 < 18; s0 += 6) {
+            uint4 x[24];
+#pragma unroll
+            for (int st = 0; st < 6; ++st)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                x[4 * st + i] = rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (s0 + st) * 64))
+                                      : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int v = 0; v < 24; ++v) {
+              const uint4 y = x[v];
+              const float m = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(y.x)), fabsf(bf16_hi(y.x))),
+                                          fmaxf(fabsf(bf16_lo(y.y)), fabsf(bf16_hi(y.y)))),
+                                    fmaxf(fmaxf(fabsf(bf16_lo(y.z)), fabsf(bf16_hi(y.z))),
+                                          fmaxf(fabsf(bf16_lo(y.w)), fabsf(bf16_hi(y.w)))));
+              am[v & 3] = fmaxf(am[v & 3], m);
+            }
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], 1));
+            am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], 2));
+          }
+          // row `lane` of the warp was read by lanes 4 * (lane & 7) + 0..3, as its (lane >> 3)-th row
+          const int src = 4 * (lane & 7);
+          const float v0 = __shfl_sync(0xffffffffu, am[0], src), v1 = __shfl_sync(0xffffffffu, am[1], src);
+          const float v2 = __shfl_sync(0xffffffffu, am[2], src), v3 = __shfl_sync(0xffffffffu, am[3], src);
+          const int sel = lane >> 3;
+          const float amax = sel == 0 ? v0 : (sel == 1 ? v1 : (sel == 2 ? v2 : v3));
           int k = 0;
           while (k < 126 && amax * ldexpf(1.f, -k) > 16384.f) ++k;
           qs = ldexpf(1.f, -k);
           qm = ldexpf(1.f, k);
         }
-        for (int c2 = 0; c2 < 9; c2 += 2) {  // two 64-channel chunks of loads in flight
-          uint4 x[16];
+        for (int s0 = 0; s0 < 18; s0 += 6) {
+          uint4 x[24];
 #pragma unroll
-          for (int v = 0; v < 16; ++v)
-            x[v] = (valid && (c2 + (v >> 3)) < 9) ? __ldg(row + c2 * 8 + v) : make_uint4(0, 0, 0, 0);
+          for (int st = 0; st < 6; ++st)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (c2 + h >= 9) break;
-            uint32_t w[32];
+            for (int i = 0; i < 4; ++i)
+              x[4 * st + i] =
+                  rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (s0 + st) * 64)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              uint4 y = x[8 * h + v];
+          for (int st = 0; st < 6; ++st) {
+            // staging row rr at rr * 64, its 16-byte chunk c at (c ^ ((rr >> 1) & 3)) (no bank conflicts)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = rsub + 8 * i;
+              *reinterpret_cast<uint4*>(qst + rr * 64 + ((csub ^ ((rr >> 1) & 3)) << 4)) = x[4 * st + i];
+            }
+            __syncwarp();
+            uint32_t w[16];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint4 y = *reinterpret_cast<const uint4*>(qst + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4));
               if (kFp8) {
                 y.x = pack_f16x2(bf16_lo(y.x) * qs, bf16_hi(y.x) * qs);
                 y.y = pack_f16x2(bf16_lo(y.y) * qs, bf16_hi(y.y) * qs);
                 y.z = pack_f16x2(bf16_lo(y.z) * qs, bf16_hi(y.z) * qs);
                 y.w = pack_f16x2(bf16_lo(y.w) * qs, bf16_hi(y.w) * qs);
               }
-              w[4 * v + 0] = y.x;
-              w[4 * v + 1] = y.y;
-              w[4 * v + 2] = y.z;
-              w[4 * v + 3] = y.w;
+              w[4 * c4 + 0] = y.x;
+              w[4 * c4 + 1] = y.y;
+              w[4 * c4 + 2] = y.z;
+              w[4 * c4 + 3] = y.w;
             }
-            tmem_st32(tbase + lane_off + kColQ + 32 * (c2 + h), w);
+            __syncwarp();
+            tmem_st16(tbase + lane_off + kColQ + 16 * (s0 + st), w);
           }
         }
         tmem_wait_st();
@@ -503,13 +576,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       };
 
       while (ok && it.next(s)) {
+        if (s.empty) continue;  // the accumulator writes its zero output and lse
         const int r = s.rb * kRowsPerBlock + L;
         const bool row_valid = r < a.R;
-        const size_t out_row = static_cast<size_t>(s.b) * a.R + r;
-        if (s.empty) {
-          if (row_valid) a.lse[out_row] = -INFINITY;
-          continue;
-        }
         const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
         int n_vis = 0;
         if (row_valid) {
@@ -522,6 +591,22 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
+          if (j == max(s.page_lo, s.page_hi - 3)) {
+            // the next segment's Q row of this thread into L2 (plain prefetches,
+            // so the TMA unit stays free for pages)
+            SegIter look = it;
+            Seg nx;
+            while (look.next(nx))
+              if (!nx.empty) {
+                const int rn = nx.rb * kRowsPerBlock + L;
+                if (rn < a.R) {
+                  const uint8_t* row = reinterpret_cast<const uint8_t*>(a.q + (static_cast<size_t>(nx.b) * a.R + rn) * kDqk);
+#pragma unroll
+                  for (int v = 0; v < 9; ++v) prefetch_line_l2(row + 128 * v);
+                }
+                break;
+              }
+          }
           if (!mbar_wait(smem_u32(&bars->s_full[sb]), sph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           float x[64];
@@ -579,6 +664,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
         if (!ok) break;
 
+        // the row sum and lse go to the accumulator, which writes the outputs
+        const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+        if (!mbar_wait(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        st_async_v2_f32(rL + L * 8, l, lse_v, rLfull);
+        ++seg_n;
+
         // Q of the next segment with pages can go in now (its QK overlaps the
         // accumulator's last PV and epilogue of this one).
         {
@@ -592,35 +683,30 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             }
           }
         }
-
-        // lse here; the row sum goes to the accumulator for its epilogue
-        const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
-        if (row_valid) {
-          if (s.split)
-            a.lse_part[static_cast<size_t>(s.slot) * kRowsPerBlock + L] = lse_v;
-          else
-            a.lse[out_row] = lse_v;
-        }
-        const uint32_t lb = seg_n & 1u, lph = (seg_n >> 1) & 1u;
-        if (!mbar_wait(smem_u32(&bars->l_free[lb]), lph ^ 1u, abort_flag)) { ok = false; break; }
-        st_async_f32(rL + lb * kVecBytes + L * 4, l, lb ? rLfull1 : rLfull0);
-        ++seg_n;
       }
     } else {
       // ------------------------------------------------------------ rescale + epilogue (accumulator)
       const float* alpha_s = reinterpret_cast<const float*>(smem + kOffAlpha);
-      const float* l_s = reinterpret_cast<const float*>(smem + kOffL);
-      const uint32_t rLfree0 = mapa_shared(smem_u32(&bars->l_free[0]), peer);
-      const uint32_t rLfree1 = mapa_shared(smem_u32(&bars->l_free[1]), peer);
-      uint32_t ofull_ph = 0;
+      const float2* l_s = reinterpret_cast<const float2*>(smem + kOffL);
+      const uint32_t rLfree = mapa_shared(smem_u32(&bars->l_free), peer);
+      const uint32_t rPfree0 = mapa_shared(smem_u32(&bars->pbuf_free[0]), peer);
+      const uint32_t rPfree1 = mapa_shared(smem_u32(&bars->pbuf_free[1]), peer);
+      uint32_t ofull_ph = 0, epi_ph = 0, mrg_n = 0;
+      auto epi_sync = [&]() -> bool {
+        mbar_arrive(smem_u32(&bars->epi_bar));
+        const bool done = mbar_wait(smem_u32(&bars->epi_bar), epi_ph, abort_flag);
+        epi_ph ^= 1u;
+        return done;
+      };
       while (ok && it.next(s)) {
         const int r = s.rb * kRowsPerBlock + L;
         const bool row_valid = r < a.R;
         const size_t out_row = static_cast<size_t>(s.b) * a.R + r;
-        if (s.empty) {
+        if (s.empty) {  // no visible keys: zero output, lse -inf
           if (row_valid) {
             uint4* o = reinterpret_cast<uint4*>(a.out + out_row * kDv);
             for (int v = 0; v < kDv / 8; ++v) o[v] = make_uint4(0, 0, 0, 0);
+            a.lse[out_row] = -INFINITY;
           }
           continue;
         }
@@ -649,52 +735,247 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
         if (!ok) break;
 
-        // epilogue: O / l -> out (bf16) or the fp32 partial slot
+        // ---- epilogue.  Three cases:
+        //  0  the unit is not split: O / l -> out (bf16), lse -> lse;
+        //  1  a piece of a split unit: O / l (fp16, row-scaled) and lse -> its
+        //     partial slot; when the unit has at most kFuseMax pieces, a ready
+        //     flag follows;
+        //  2  the last piece to finish of a unit with at most kFuseMax pieces:
+        //     merges the other pieces' partials with its own O (the LSE merge)
+        //     and writes out and lse itself.
         if (!mbar_wait(smem_u32(&bars->o_full), ofull_ph, abort_flag)) { ok = false; break; }
         ofull_ph ^= 1u;
-        const uint32_t lb = seg_n & 1u, lph = (seg_n >> 1) & 1u;
-        if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->l_full[lb]), kVecBytes);
-        if (!mbar_wait<true>(smem_u32(&bars->l_full[lb]), lph, abort_flag)) { ok = false; break; }
-        const float l = l_s[lb * kRowsPerBlock + L];
+        if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->l_full), kRowsPerBlock * 8);
+        if (!mbar_wait<true>(smem_u32(&bars->l_full), seg_n & 1u, abort_flag)) { ok = false; break; }
+        const float2 lrow = l_s[L];  // (row sum, lse) of this piece
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(lb ? rLfree1 : rLfree0);
+        if (lane == 0) mbar_arrive_remote(rLfree);
         ++seg_n;
+        const float l = lrow.x, lse_own = lrow.y;
+        int mode = 0, c0 = 0, k = 1, first = 0;
+        if (s.split) {
+          const int p0 = __ldg(a.pre + s.u), p1 = __ldg(a.pre + s.u + 1);
+          first = p0 + a.overhead;
+          c0 = first / W;
+          k = (p1 - 1) / W - c0 + 1;
+          mode = 1;
+          if (k <= kFuseMax) {
+            if (ctid == 0) bars->ticket = atomicAdd(a.unit_cnt + c0, 1);
+            if (!epi_sync()) { ok = false; break; }
+            if (*reinterpret_cast<volatile int*>(&bars->ticket) == k - 1) mode = 2;
+          }
+        }
+        // partial slot of piece i (cluster c0 + i) of this unit
+        auto piece_slot = [&](int i) { return (i == 0 && first != c0 * W) ? 2 * c0 + 1 : 2 * (c0 + i); };
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        for (int ch = 0; ch < 16; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(tbase + lane_off + 32 * ch, o);
-          tmem_wait_ld();
-          if (row_valid) {
-            if (s.split) {
-              float4* dst = reinterpret_cast<float4*>(a.o_part + (static_cast<size_t>(s.slot) * kRowsPerBlock + L) * kDv +
-                                                      32 * ch);
+        // Final rows go through the P buffer of the segment's last tile (its PV
+        // is done; its credit goes back to the scorer only after this).
+        const uint32_t last_sb = (t - 1u) & 1u;
+        uint8_t* const est = smem + kOffP + last_sb * kPBytes + wq * (kPBytes / 4);
+        uint16_t* const dst = a.out + (static_cast<size_t>(s.b) * a.R + s.rb * kRowsPerBlock + wq * 32) * kDv;
+        const int rows_left = a.R - (s.rb * kRowsPerBlock + wq * 32);  // rows of this warp inside the request
+        if (mode == 1) {
+          // fp16 partial O / l, scaled by a power of two that puts the row's
+          // largest magnitude in [2^14, 2^15) (lse_part holds the scale): every
+          // bf16-representable value within 2^-29 of the row maximum is stored
+          // exactly, and nothing can overflow.  Chunk-interleaved slot: thread
+          // L writes 8-channel chunk j of its row at [j][L], so each store
+          // instruction covers 512 contiguous bytes.
+          const float inv_l = l > 0.f ? 1.f / l : 0.f;
+          float amax = 0.f;
+          for (int ch = 0; ch < 16; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(tbase + lane_off + 32 * ch, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                     __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(a.out + out_row * kDv + 32 * ch);
+            for (int v = 0; v < 32; ++v) amax = fmaxf(amax, fabsf(__uint_as_float(o[v])));
+          }
+          float sc = 1.f;
+          if (amax * inv_l > 0.f) {
+            int e2;
+            frexpf(amax * inv_l, &e2);  // amax / l < 2^e2
+            sc = ldexpf(1.f, max(-120, min(120, e2 - 15)));
+          }
+          const float f = inv_l / sc;
+          uint4* part = reinterpret_cast<uint4*>(a.o_part) + static_cast<size_t>(s.slot) * kPartChunks * kRowsPerBlock + L;
+          for (int ch = 0; ch < 16; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(tbase + lane_off + 32 * ch, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-                w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-                w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-                w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-                dst[v] = w;
+            for (int q = 0; q < 4; ++q)
+              part[static_cast<size_t>(4 * ch + q) * kRowsPerBlock] =
+                  make_uint4(pack_f16x2(__uint_as_float(o[8 * q + 0]) * f, __uint_as_float(o[8 * q + 1]) * f),
+                             pack_f16x2(__uint_as_float(o[8 * q + 2]) * f, __uint_as_float(o[8 * q + 3]) * f),
+                             pack_f16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f),
+                             pack_f16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f));
+          }
+          reinterpret_cast<float2*>(a.lse_part)[static_cast<size_t>(s.slot) * kRowsPerBlock + L] = make_float2(lse_own, sc);
+          __threadfence();  // the partial is visible GPU-wide before its ready flag
+        } else if (mode == 0) {
+          const float inv_l = l > 0.f ? 1.f / l : 0.f;
+          for (int cc = 0; cc < 8; ++cc) {
+            float v[64];
+            {
+              uint32_t o0[32], o1[32];
+              tmem_ld32(tbase + lane_off + 64 * cc, o0);
+              tmem_ld32(tbase + lane_off + 64 * cc + 32, o1);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] = __uint_as_float(o0[i]) * inv_l;
+                v[32 + i] = __uint_as_float(o1[i]) * inv_l;
               }
             }
+            store_rows_bf16(est, v, dst, rows_left, cc, lane);
+          }
+          if (row_valid) a.lse[out_row] = lse_own;
+        } else {
+          // wait for the other pieces' partials (they hold tickets, so they are
+          // in their epilogues and never wait on anything outside their cluster)
+          if (ctid == 0) {
+            for (int i = 0; i < k; ++i)
+              if (c0 + i != c && !wait_flag_gpu(a.slot_ready + piece_slot(i))) atomicOr(a.err, kErrTimeout);
+          }
+          if (!epi_sync()) { ok = false; break; }
+          // lse_total = ln(sum_i exp(lse_i)); out = sum_i exp(lse_i - lse_total) * out_i,
+          // with out_own = O / l and out_i = stored_i * scale_i
+          float lse_i[kFuseMax], sc_i[kFuseMax];
+          float mx = lse_own;
+#pragma unroll
+          for (int i = 0; i < kFuseMax; ++i) {
+            lse_i[i] = -INFINITY;
+            sc_i[i] = 0.f;
+            if (i < k && c0 + i != c) {
+              const float2 ls = __ldcg(reinterpret_cast<const float2*>(a.lse_part) +
+                                       static_cast<size_t>(piece_slot(i)) * kRowsPerBlock + L);
+              lse_i[i] = ls.x;
+              sc_i[i] = ls.y;
+            }
+            mx = fmaxf(mx, lse_i[i]);
+          }
+          float c_own = 0.f, c_i[kFuseMax], lse_tot = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kFuseMax; ++i) c_i[i] = 0.f;
+          if (mx != -INFINITY) {
+            const float e_own = ex2_approx((lse_own - mx) * kLog2e);
+            float sum = e_own;
+#pragma unroll
+            for (int i = 0; i < kFuseMax; ++i) {
+              c_i[i] = ex2_approx((lse_i[i] - mx) * kLog2e);
+              sum += c_i[i];
+            }
+            const float inv = 1.f / sum;
+#pragma unroll
+            for (int i = 0; i < kFuseMax; ++i) c_i[i] *= inv * sc_i[i];
+            c_own = l > 0.f ? e_own * inv / l : 0.f;
+            lse_tot = mx + lg2_approx(sum) * kLn2;
+          }
+          // At the cluster's last segment the page ring is idle: each other
+          // piece's partial (128 KB) comes in with one round of bulk copies and
+          // is read from shared memory.  Otherwise it is read from global
+          // memory directly.  With several other pieces, the running result
+          // is kept in O (TMEM) between passes.
+          bool ring_free = true;
+          {
+            SegIter look = it;
+            Seg nx;
+            while (look.next(nx))
+              if (!nx.empty) {
+                ring_free = false;
+                break;
+              }
+          }
+          const int own = c - c0;
+          for (int pi = 0; pi < k - 1 && ok; ++pi) {
+            const int i = pi < own ? pi : pi + 1;
+            float cf = 0.f;
+#pragma unroll
+            for (int x = 0; x < kFuseMax; ++x)
+              if (x == i) cf = c_i[x];
+            const uint4* gsrc = reinterpret_cast<const uint4*>(a.o_part) +
+                                static_cast<size_t>(piece_slot(i)) * kPartChunks * kRowsPerBlock;
+            const uint4* src = gsrc + L;
+            if (ring_free) {
+              if (ctid == 0) {
+                const uint32_t mb = smem_u32(&bars->mrg_bar);
+                mbar_arrive_expect_tx(mb, kPartBytes);
+                for (int off = 0; off < kPartBytes; off += 32768)
+                  bulk_load(smem_u32(smem + off), reinterpret_cast<const uint8_t*>(gsrc) + off, 32768, mb);
+              }
+              if (!mbar_wait(smem_u32(&bars->mrg_bar), mrg_n & 1u, abort_flag)) { ok = false; break; }
+              ++mrg_n;
+              src = reinterpret_cast<const uint4*>(smem) + L;
+            }
+            const bool first_pass = pi == 0, last_pass = pi == k - 2;
+            for (int cc = 0; cc < 8; ++cc) {
+              float v[64];
+              {
+                uint32_t o0[32], o1[32];
+                tmem_ld32(tbase + lane_off + 64 * cc, o0);
+                tmem_ld32(tbase + lane_off + 64 * cc + 32, o1);
+                tmem_wait_ld();
+                const float m = first_pass ? c_own : 1.f;
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                  v[x] = __uint_as_float(o0[x]) * m;
+                  v[32 + x] = __uint_as_float(o1[x]) * m;
+                }
+              }
+              uint4 w[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                w[q] = ring_free ? src[static_cast<size_t>(8 * cc + q) * kRowsPerBlock]
+                                 : __ldcg(src + static_cast<size_t>(8 * cc + q) * kRowsPerBlock);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const uint32_t ww[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&ww[h]));
+                  v[8 * q + 2 * h] += cf * f2.x;
+                  v[8 * q + 2 * h + 1] += cf * f2.y;
+                }
+              }
+              if (last_pass) {
+                store_rows_bf16(est, v, dst, rows_left, cc, lane);
+              } else {
+                uint32_t o0[32], o1[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                  o0[x] = __float_as_uint(v[x]);
+                  o1[x] = __float_as_uint(v[32 + x]);
+                }
+                tmem_st32(tbase + lane_off + 64 * cc, o0);
+                tmem_st32(tbase + lane_off + 64 * cc + 32, o1);
+              }
+            }
+            if (!last_pass) tmem_wait_st();
+            if (ring_free && !last_pass && !epi_sync()) { ok = false; break; }  // ring read before the next copy
+          }
+          if (!ok) break;
+          if (row_valid) a.lse[out_row] = lse_tot;
+          if (ctid == 0) {  // leave the flags and the counter clear for the next call
+            for (int i = 0; i < k; ++i)
+              if (c0 + i != c) a.slot_ready[piece_slot(i)] = 0;
+            a.unit_cnt[c0] = 0;
           }
         }
         tc_fence_before();
+        if (!epi_sync()) { ok = false; break; }  // all four warps are done with the staging buffer
+        if (ctid == 0) {
+          mbar_arrive_remote(last_sb ? rPfree1 : rPfree0);
+          if (mode == 1 && k <= kFuseMax) st_release_gpu(a.slot_ready + s.slot, 1);
+        }
         mbar_arrive(smem_u32(&bars->o_free));
       }
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
   } else if (warp == 6) {
     // ---------------------------------------------------------------- credit relay (accumulator)
-    // After PV of tile t, P buffer t%2 may be refilled by the scorer.
+    // After PV of tile t, P buffer t%2 may be refilled by the scorer; the
+    // buffer of a segment's last tile is returned by the epilogue instead,
+    // which stages its stores there.
     if (!scorer && lane == 0) {
       const uint32_t rFree0 = mapa_shared(smem_u32(&bars->pbuf_free[0]), peer);
       const uint32_t rFree1 = mapa_shared(smem_u32(&bars->pbuf_free[1]), peer);
@@ -707,7 +988,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t & 1u;
           if (!mbar_wait(smem_u32(&bars->pv_done[sb]), (t >> 1) & 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_remote(sb ? rFree1 : rFree0);
+          if (j + 1 < s.page_hi) mbar_arrive_remote(sb ? rFree1 : rFree0);
         }
       }
       if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
@@ -811,7 +1092,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
 int decode_smem_bytes(bool) { return kSmem; }
 
-static cudaLaunchConfig_t make_cfg(bool fp8, int clusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
+static cudaLaunchConfig_t make_cfg(bool fp8, int clusters, cudaStream_t stream, cudaLaunchAttribute* attr,
+                                   bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(fp8 ? Cfg<true>::kThreads : Cfg<false>::kThreads, 1, 1);
@@ -821,8 +1103,11 @@ static cudaLaunchConfig_t make_cfg(bool fp8, int clusters, cudaStream_t stream, 
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the prologue may overlap the planner
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cfg;
 }
 
@@ -834,20 +1119,20 @@ static cudaError_t set_smem_attr(bool fp8) {
 cudaError_t decode_max_active_clusters(bool fp8, int* clusters) {
   cudaError_t e = set_smem_attr(fp8);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_cfg(fp8, 1, nullptr, attr);
   if (fp8) return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<true>, &cfg);
   return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<false>, &cfg);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map, int clusters, bool fp8,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map9, const CUtensorMap& kv_map8,
+                          int clusters, bool fp8, cudaStream_t stream) {
   cudaError_t e = set_smem_attr(fp8);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg(fp8, clusters, stream, attr);
-  if (fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map, a);
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map, a);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = make_cfg(fp8, clusters, stream, attr, true);
+  if (fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map9, kv_map8, a);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map9, kv_map8, a);
 }
 
 }  // namespace mla_gb300

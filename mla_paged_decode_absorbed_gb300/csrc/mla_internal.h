@@ -12,12 +12,19 @@ constexpr int kDv = 512;             // output channels (latent part of a KV row
 constexpr int kRowsPerBlock = 128;   // query rows (token-major (i, h)) per work unit = MMA M
 constexpr int kGroups = 5;           // fp8 scale groups per token
 constexpr int kDefaultOverhead = 2;  // planner cost per work unit, in pages
+// A split unit with at most this many pieces is merged inside the attention
+// kernel by the piece that finishes last; units with more pieces are merged by
+// the combine kernel.
+constexpr int kFuseMax = 4;
+// Partial slots hold fp16 O / l in 8-channel chunks: [slot][kPartChunks][128 rows][8].
+constexpr int kPartChunks = 512 / 8;
 
 // Device error bits in workspace word 0.
 enum : int32_t { kErrBounds = 1, kErrTimeout = 2, kErrRange = 4 };
 
 // Workspace header words (int32).
-enum : int { kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters = 4, kHdrOvh = 5 };
+// kHdrCombine: 1 if some unit has more than kFuseMax pieces (the combine kernel has work).
+enum : int { kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters = 4, kHdrOvh = 5, kHdrCombine = 6 };
 
 struct DecodeArgs {
   const uint16_t* q;          // bf16 [B, s_q, H, 576]
@@ -30,8 +37,10 @@ struct DecodeArgs {
   const int32_t* pre;         // [units + 1]
   uint16_t* out;              // bf16 [B, s_q, H, 512]
   float* lse;                 // [B, s_q, H]
-  float* o_part;              // [2 * clusters, 128, 512]
-  float* lse_part;            // [2 * clusters, 128]
+  void* o_part;               // fp16 [2 * clusters][64 chunks of 8 channels][128 rows][8]
+  float* lse_part;            // [2 * clusters, 128, 2]: (lse, power-of-two scale of the stored values)
+  int32_t* unit_cnt;          // [clusters]: pieces finished of the split unit whose pages start in cluster c
+  int32_t* slot_ready;        // [2 * clusters]: partial slot written (1) / consumed (0)
   int32_t* err;               // workspace word 0
   int B, s_q, H, R, n_rb, U, num_pages, max_pages, overhead;
   float scale_log2;           // softmax_scale * log2(e)
@@ -41,7 +50,7 @@ struct CombineArgs {
   const int32_t* hdr;
   const int32_t* cl_first;
   const int32_t* pre;
-  const float* o_part;
+  const void* o_part;
   const float* lse_part;
   uint16_t* out;
   float* lse;
@@ -51,7 +60,11 @@ struct CombineArgs {
 // mla_decode_kernel.cu
 int decode_smem_bytes(bool fp8);
 cudaError_t decode_max_active_clusters(bool fp8, int* clusters);
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map, int clusters, bool fp8,
-                          cudaStream_t stream);
+// kv_map9 / kv_map8: the cache as a 4-D tensor (64 channels, 64 tokens, 9
+// channel chunks, pages) with a chunk stride of 128 bytes; one box brings
+// chunks 0..8 (scorer) or 0..7 (accumulator) of a page, laid out in shared
+// memory as consecutive 64-token x 64-channel swizzled blocks.
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map9, const CUtensorMap& kv_map8,
+                          int clusters, bool fp8, cudaStream_t stream);
 
 }  // namespace mla_gb300

@@ -84,6 +84,12 @@ class Plan:
             out.append(Piece(u, b, rb, lo - a, hi - a, split, slot))
         return out
 
+    def piece_count(self, u: int) -> int:
+        """Number of clusters unit u's pages fall in (0 for a unit with no pages)."""
+        if self.tiles[u] == 0:
+            return 0
+        return len({c for c in range(self.G) for p in self.pieces(c) if p.unit == u})
+
     def combine_unit(self, c: int):
         """(unit, [(cluster, slot), ...]) the combine step of cluster c merges, or None."""
         lo_c, hi_c = c * self.W, (c + 1) * self.W

@@ -56,8 +56,9 @@ def test_workspace_size_is_host_only(lib):
     n = mla.mla_workspace_size(d, 152)
     lay = mla.mla_get_workspace_layout(d, 76)
     assert n == lay.total and n % 256 == 0
-    assert lay.o_part >= lay.lse_part >= lay.pre >= lay.cl_first >= lay.header
-    assert lay.total - lay.o_part >= 2 * 76 * 128 * 512 * 4
+    assert lay.o_part >= lay.lse_part >= lay.sync >= lay.pre >= lay.cl_first >= lay.header
+    assert lay.lse_part - lay.sync >= 3 * 76 * 4
+    assert lay.total - lay.o_part >= 2 * 76 * 128 * 512 * 2
     # capping clusters shrinks the partial buffers
     assert mla.mla_workspace_size(_desc(max_clusters=4), 152) < n
 

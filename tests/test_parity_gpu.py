@@ -186,9 +186,11 @@ def test_device_plan_equals_reference_plan(seqlens, heads, s_q, clusters, ovh):
     torch.cuda.synchronize()
     lay = mla.mla_get_workspace_layout(d, G)
     w = ws.cpu()
-    hdr = w[lay.header:lay.header + 24].view(torch.int32).tolist()
+    hdr = w[lay.header:lay.header + 28].view(torch.int32).tolist()
     ref = plan_ref.make_plan(seqlens, s_q, heads, inp.max_pages_per_seq, G, ovh or 2)
-    assert hdr == [0, ref.W, ref.pre[-1], ref.units, G, ref.overhead]
+    many = int(any(ref.piece_count(u) > 4 for u in range(ref.units)))
+    assert hdr == [0, ref.W, ref.pre[-1], ref.units, G, ref.overhead, many]
+    assert w[lay.sync:lay.sync + 12 * G].view(torch.int32).eq(0).all()
     pre = w[lay.pre:lay.pre + 4 * (ref.units + 1)].view(torch.int32).tolist()
     assert pre == ref.pre
     cl_first = w[lay.cl_first:lay.cl_first + 4 * G].view(torch.int32).tolist()
@@ -253,3 +255,44 @@ def test_side_stream_and_cuda_graph_replay():
     torch.cuda.synchronize()
     assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
     assert dec.device_error() == mla.MLA_OK
+
+
+# ------------------------------------------------------------------ split merges
+@pytest.mark.parametrize("clusters", [3, 5, 12, 40])
+def test_merge_in_kernel_and_in_combine(clusters):
+    """Units split into 2..4 pieces are merged by the attention kernel's last
+    finisher; units with more pieces by the combine kernel.  Both must match."""
+    seqlens = [9000, 64, 3100, 700, 1, 2000]
+    inp = gen.make_inputs("x", seqlens=seqlens, heads=128, s_q=1, seed=40 + clusters)
+    d = mla.make_desc(inp.batch, 1, 128, inp.num_pages, inp.max_pages_per_seq, max_clusters=clusters)
+    G = mla.mla_num_clusters(d)
+    ref = plan_ref.make_plan(seqlens, 1, 128, inp.max_pages_per_seq, G, 2)
+    counts = {ref.piece_count(u) for u in range(ref.units)}
+    assert counts & {2, 3, 4} or max(counts) > 4, counts
+    _check(inp, max_clusters=clusters)
+
+
+def test_attention_rerun_without_replanning():
+    """The attention kernel leaves the merge counters and slot flags clear, so
+    plan once, then attention + combine twice gives the same result."""
+    inp = gen.make_inputs("x", seqlens=[5000, 2500, 300], heads=128, s_q=1, seed=77)
+    q, kv, sc, bt, sl = to_device(inp)
+    d = mla.make_desc(inp.batch, 1, 128, inp.num_pages, inp.max_pages_per_seq, max_clusters=9)
+    ws = mla.alloc_workspace(d)
+    G = mla.mla_num_clusters(d)
+    lay = mla.mla_get_workspace_layout(d, G)
+    outs = []
+    mla.mla_plan(d, sl, ws)
+    for _ in range(2):
+        out = torch.zeros((inp.batch, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros((inp.batch, 1, 128), dtype=torch.float32, device="cuda")
+        mla.mla_decode_attention(d, q, kv, None, bt, sl, 1, inp.softmax_scale, out, lse, ws)
+        mla.mla_combine(d, out, lse, ws)
+        torch.cuda.synchronize()
+        assert ws[lay.sync:lay.sync + 12 * G].view(torch.int32).eq(0).all()
+        outs.append((out.clone(), lse.clone()))
+    assert mla.mla_get_device_error(ws) == mla.MLA_OK
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    out_r, lse_r = oracle.mla_decode_inputs(inp)
+    compare(outs[0][0].float().cpu().numpy().reshape(-1, 512).astype(np.float64),
+            outs[0][1].cpu().numpy().reshape(-1).astype(np.float64), out_r, lse_r, TOL_BF16)

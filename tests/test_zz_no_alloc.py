@@ -51,6 +51,6 @@ def test_noalloc_matches_workspace_path_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_what_the_scratch_cannot_hold():
-    d = mla.make_desc(4096, 16, 1024, 10, 1)      # 524,288 (row block, request) units
+    d = mla.make_desc(65536, 16, 1024, 10, 1)     # 8,388,608 (row block, request) units
     st = mla.noalloc_function()(ctypes.byref(d), 256, 256, None, 256, 256, 16, 0.07, 256, 256, 0, None)
     assert st == mla.MLA_ERR_WORKSPACE
