@@ -62,6 +62,34 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+KERNEL_SOURCES = ("mla_paged_decode_absorbed_gb300/csrc/mla_decode_kernel.cu",
+                  "mla_paged_decode_absorbed_gb300/csrc/sm103_ptx.cuh",
+                  "mla_paged_decode_absorbed_gb300/csrc/mla_internal.h")
+NCU_SUMMARY = {"decode": "profiles/mla_decode_kernel_B64_H128_ncu_full.md"}
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary of this workload, or None when there is none or the kernel
+    sources changed since it was captured (sha256 recorded beside it)."""
+    import hashlib
+    name = NCU_SUMMARY.get(workload)
+    if name is None:
+        return None
+    try:
+        text = open(os.path.join(ROOT, name)).read()
+        h = hashlib.sha256()
+        for f in KERNEL_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        fields = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith(("dram_bytes", "kernel_source")))
+        if fields.get("kernel_source_sha256", "").strip() != h.hexdigest():
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def work_of(inp):
     """(flops, kv_bytes) of one call: per row the visible keys, per request the
     cache bytes of the tokens the longest row sees."""
@@ -370,7 +398,7 @@ def main():
     if hbm_bound:
         roof = {"kernel": "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>", "bound": "hbm",
                 "achieved": k_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": k_gbs / hbm_gbs,
-                "traffic": None, "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
+                "traffic": measured_traffic(args.workload), "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
                 "algorithmic_bytes_per_launch": kv_bytes}
     else:
         roof = {"kernel": "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>", "bound": "tensor",
