@@ -309,6 +309,56 @@ mla_status make_kv_map4(const void* kv, int num_pages, int chunks, CUtensorMap* 
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
+// q [B, R, 576] bf16 as a 4-D tensor (64 channels, 9 chunks, R rows, B): one
+// box (64, 9, 64, 1) is half a 128-row block (72 KB), 128-byte swizzled; rows
+// past R read as zeros.
+mla_status make_q_map(const void* q, int B, int R, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  cuuint64_t dims[4] = {64, 9, static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {128, kDqk * 2, static_cast<cuuint64_t>(R) * kDqk * 2};
+  cuuint32_t box[4] = {64, 9, kRowsPerBlock / 2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
+// out [B, R, 512] bf16 as a 3-D tensor: one box (64, 32, 1) is 32 rows x 64
+// channels, 128-byte swizzled; rows past R are not written.
+mla_status make_out_map(void* out, int B, int R, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDv), static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {kDv * 2, static_cast<cuuint64_t>(R) * kDv * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
+// out as a 4-D tensor (64 channels, R rows, 8 channel chunks, B): one box
+// (64, 32, 4, 1) is 32 rows x 256 channels, stored from shared memory as 4
+// chunk-major blocks of 32 x 128-byte swizzled rows.
+mla_status make_out_map4(void* out, int B, int R, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(R), 8, static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {kDv * 2, 128, static_cast<cuuint64_t>(R) * kDv * 2};
+  cuuint32_t box[4] = {64, 32, 4, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
 struct Prepared {
   Dims x;
   DeviceInfo di;
@@ -367,6 +417,11 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
     if (st == MLA_OK) st = make_kv_map4(kv, p.x.P, 8, &map8);
     if (st != MLA_OK) return st;
   }
+  CUtensorMap qmap, omap, omap4;
+  mla_status st = make_q_map(q, p.x.B, p.x.R, &qmap);
+  if (st == MLA_OK) st = make_out_map(out, p.x.B, p.x.R, &omap);
+  if (st == MLA_OK) st = make_out_map4(out, p.x.B, p.x.R, &omap4);
+  if (st != MLA_OK) return st;
   DecodeArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.kv = kv;
@@ -393,7 +448,7 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   a.max_pages = p.x.maxp;
   a.overhead = p.x.ovh;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(launch_decode(a, map9, map8, p.G, p.x.fp8, stream));
+  return launch_status(launch_decode(a, map9, map8, qmap, omap, omap4, p.G, p.x.fp8, stream));
 }
 
 mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t stream) {

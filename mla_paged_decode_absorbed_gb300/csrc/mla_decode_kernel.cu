@@ -92,6 +92,8 @@ struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t q_full;        // scorer: Q written to TMEM (softmax warps, 128)
+  uint64_t q_tma;         // scorer: first segment's Q block arrived in ring stages 1-2 (1 + tx)
+  uint64_t q_smem_free;   // scorer: that Q block was read, stages 1-2 may take pages (128)
   uint64_t s_full[2];     // scorer: QK done (commit)
   uint64_t s_free[2];     // scorer: S read by the softmax (128)
   uint64_t pbuf_free[2];  // scorer: accumulator finished with P tile b (remote, 1)
@@ -185,13 +187,14 @@ __device__ __forceinline__ void zero_tail_rows(uint8_t* stage, int valid, int nb
   fence_proxy_async_smem();
 }
 
-// Writes output channels [64*cc, 64*cc + 64) of a warp's 32 rows: thread
-// `lane` holds row `lane` (64 final values).  The rows are staged through
-// `est` (4 KB, 16-byte chunks XOR-swizzled by row) so that each store
-// instruction writes four whole 128-byte lines (8 lanes per row) instead of
-// 32 scattered pieces.  Rows at or past `rows_left` are not written.
-__device__ __forceinline__ void store_rows_bf16(uint8_t* est, const float (&v)[64], uint16_t* dst, int rows_left,
-                                                int cc, int lane) {
+// Writes output channels [64*cc, 64*cc + 64) of a warp's 32 rows (rows
+// row0.. of request b): thread `lane` holds row `lane` (64 final values).  The
+// rows are staged in `est` (4 KB, 1024-aligned) in the 128-byte-swizzled
+// layout of one out_map box, and one lane hands the box to the TMA unit (rows
+// past the request are clipped by the tensor map).  The staging area is free
+// again when the call returns.
+__device__ __forceinline__ void store_rows_tma(uint8_t* est, const float (&v)[64], const CUtensorMap* out_map,
+                                               int cc, int row0, int b, int R, int lane) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     uint4 w;
@@ -201,15 +204,41 @@ __device__ __forceinline__ void store_rows_bf16(uint8_t* est, const float (&v)[6
     w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
     *reinterpret_cast<uint4*>(est + lane * 128 + ((q ^ (lane & 7)) << 4)) = w;
   }
+  fence_proxy_async_smem();
   __syncwarp();
-  const int rsub = lane >> 3, csub = lane & 7;
+  if (lane == 0 && row0 < R) {  // a warp whose rows all lie past the request stores nothing
+    tma_store_3d(out_map, 64 * cc, row0, b, smem_u32(est));
+    bulk_commit_group();
+    bulk_wait_read_all();
+  }
+  __syncwarp();
+}
+
+// Stages output channels [64*cc, 64*cc + 64) of a warp's 32 rows, cc = 4*half
+// + k, into `half_buf` (16 KB, 1024-aligned) in the layout of one out_map4
+// box: 32 rows x 4 chunks of 64 channels, row r of chunk k at line 32k + r,
+// 128-byte swizzled (no bank conflicts: the line index mod 8 is the row).
+__device__ __forceinline__ void stage_half(uint8_t* half_buf, const float (&v)[64], int k, int lane) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int rr = 4 * k + rsub;
-    if (rr < rows_left) {
-      const uint4 y = *reinterpret_cast<const uint4*>(est + rr * 128 + ((csub ^ (rr & 7)) << 4));
-      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(rr) * kDv + 64 * cc + 8 * csub) = y;
-    }
+  for (int q = 0; q < 8; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(half_buf + (k * 32 + lane) * 128 + ((q ^ (lane & 7)) << 4)) = w;
+  }
+}
+
+// One TMA store of a staged half (256 channels x 32 rows); the caller waits
+// for its reads before reusing the buffer.
+__device__ __forceinline__ void store_half(uint8_t* half_buf, const CUtensorMap* out_map4, int half, int row0,
+                                           int b, int R, int lane) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < R) {
+    tma_store_4d(out_map4, 0, row0, 4 * half, b, smem_u32(half_buf));
+    bulk_commit_group();
   }
   __syncwarp();
 }
@@ -236,7 +265,8 @@ __device__ __forceinline__ float max64(const float (&x)[64]) {
 template <bool kFp8>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map9, const __grid_constant__ CUtensorMap kv_map8,
-                      const DecodeArgs a) {
+                      const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap out_map,
+                      const __grid_constant__ CUtensorMap out_map4, const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -258,6 +288,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(smem_u32(&bars->kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars->q_full), 128);
+    mbar_init(smem_u32(&bars->q_tma), 1);
+    mbar_init(smem_u32(&bars->q_smem_free), 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
       mbar_init(smem_u32(&bars->s_free[i]), 128);
@@ -277,7 +309,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
-  if (warp == 0 && lane == 0 && !kFp8) tma_prefetch_desc(scorer ? &kv_map9 : &kv_map8);
+  if (warp == 0 && lane == 0) {
+    if (!kFp8) tma_prefetch_desc(scorer ? &kv_map9 : &kv_map8);
+    if (!kFp8 && scorer) tma_prefetch_desc(&q_map);
+    if (!scorer) {
+      tma_prefetch_desc(&out_map);
+      tma_prefetch_desc(&out_map4);
+    }
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
@@ -320,6 +359,15 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     SegIter it = it0;
     Seg s;
     const uint64_t policy = l2_policy_evict_first();
+    // bf16 scorer: the first segment's Q block (128 rows x 576 channels =
+    // exactly two ring stages) comes in by TMA right after the first page, into
+    // stages 1-2; pages go there only after the softmax warps have read it.
+    int q_tma_state = (scorer && !kFp8) ? 0 : 2;  // 0: not issued, 1: issued, 2: done
+    // At kernel start every CTA wants its first data at once (DRAM-bound).  The
+    // accumulator needs V only for its first PV, after the first P tile has
+    // arrived; waiting for that keeps its (second) reads of the first pages
+    // out of the start-up burst, so the scorer's Q and first page land sooner.
+    bool wait_first_p = !scorer && !kFp8;
     int stage = 0;
     uint32_t ph = 0;
     int last_par[kStages];
@@ -336,7 +384,21 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         const int cnt = min(32, s.page_hi - p0);
         for (int k = 0; k < cnt; ++k) {
           int pid = __shfl_sync(0xffffffffu, my_pid, k);
-          if (lane == 0) {
+          if (lane == 0 && wait_first_p) {
+            wait_first_p = false;
+            if (!mbar_wait<true>(smem_u32(&bars->p_full[0]), 0u, abort_flag)) {
+              ok = false;
+              if (!*abort_flag) signal_abort(bars, a.err, peer);
+            }
+          }
+          if (lane == 0 && ok && q_tma_state == 1) {
+            q_tma_state = 2;
+            if (!mbar_wait(smem_u32(&bars->q_smem_free), 0u, abort_flag)) {
+              ok = false;
+              if (!*abort_flag) signal_abort(bars, a.err, peer);
+            }
+          }
+          if (lane == 0 && ok) {
             if (!mbar_wait(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
               ok = false;
               if (!*abort_flag) signal_abort(bars, a.err, peer);
@@ -353,6 +415,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               else
                 tma_load_4d_hint(smem_u32(dst), &kv_map8, 0, 0, 0, pid, fb, policy);
               last_par[stage] = static_cast<int>(ph);
+              if (q_tma_state == 0) {
+                q_tma_state = 1;
+                const uint32_t qb = smem_u32(&bars->q_tma);
+                mbar_arrive_expect_tx(qb, static_cast<uint32_t>(kRowsPerBlock * kDqk * 2));
+                // two boxes of 64 rows (72 KB each, the size of a page copy)
+                tma_load_4d(smem_u32(smem + kStageS), &q_map, 0, 0, s.rb * kRowsPerBlock, s.b, qb);
+                tma_load_4d(smem_u32(smem + 2 * kStageS), &q_map, 0, 0, s.rb * kRowsPerBlock + 64, s.b, qb);
+              }
             }
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -368,6 +438,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       // wait (time-bounded only) for the loads already in flight
       for (int i = 0; i < kStages; ++i)
         if (last_par[i] >= 0) mbar_wait(smem_u32(&bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
+      if (q_tma_state >= 1) mbar_wait(smem_u32(&bars->q_tma), 0u, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -574,6 +645,36 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         mbar_arrive(smem_u32(&bars->q_full));
         return qm;
       };
+      // bf16, first segment: the Q block was brought into ring stages 1-2 by
+      // TMA (row r, chunk c at line 9r + c of the 128-byte-swizzled box); each
+      // thread reads its row, frees the stages, and writes TMEM.
+      auto load_q_tma = [&]() -> bool {
+        if (!mbar_wait(smem_u32(&bars->q_tma), 0u, abort_flag)) return false;
+        const uint8_t* qs_base = smem + kStageS;
+        for (int c2 = 0; c2 < 9; c2 += 3) {
+          uint32_t w[3][32];
+#pragma unroll
+          for (int h = 0; h < 3; ++h) {
+            const int n = 9 * L + c2 + h;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 y = *reinterpret_cast<const uint4*>(qs_base + n * 128 + ((k ^ (n & 7)) << 4));
+              w[h][4 * k + 0] = y.x;
+              w[h][4 * k + 1] = y.y;
+              w[h][4 * k + 2] = y.z;
+              w[h][4 * k + 3] = y.w;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 3; ++h) tmem_st32(tbase + lane_off + kColQ + 32 * (c2 + h), w[h]);
+        }
+        mbar_arrive(smem_u32(&bars->q_smem_free));  // this thread's reads are in registers
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->q_full));
+        return true;
+      };
+      bool first_q_tma = !kFp8;
 
       while (ok && it.next(s)) {
         if (s.empty) continue;  // the accumulator writes its zero output and lse
@@ -585,7 +686,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           n_vis = seqlen - a.s_q + r / a.H + 1;
           n_vis = n_vis < 0 ? 0 : (n_vis > seqlen ? seqlen : n_vis);
         }
-        qmul = q_loaded ? qmul_next : load_q(s);
+        if (first_q_tma) {
+          first_q_tma = false;
+          if (!load_q_tma()) { ok = false; break; }
+          qmul = 1.f;
+        } else {
+          qmul = q_loaded ? qmul_next : load_q(s);
+        }
         q_loaded = 0;
         const float row_scale = a.scale_log2 * qmul;
         float m_ref = -INFINITY, l = 0.f;
@@ -767,13 +874,24 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
         // partial slot of piece i (cluster c0 + i) of this unit
         auto piece_slot = [&](int i) { return (i == 0 && first != c0 * W) ? 2 * c0 + 1 : 2 * (c0 + i); };
+        // At the cluster's last segment the page ring is idle (all its pages
+        // were consumed by the last PV and nothing more is loaded).
+        bool ring_free = true;
+        {
+          SegIter look = it;
+          Seg nx;
+          while (look.next(nx))
+            if (!nx.empty) {
+              ring_free = false;
+              break;
+            }
+        }
+        const int row0 = s.rb * kRowsPerBlock + wq * 32;
         tc_fence_after();
         // Final rows go through the P buffer of the segment's last tile (its PV
         // is done; its credit goes back to the scorer only after this).
         const uint32_t last_sb = (t - 1u) & 1u;
         uint8_t* const est = smem + kOffP + last_sb * kPBytes + wq * (kPBytes / 4);
-        uint16_t* const dst = a.out + (static_cast<size_t>(s.b) * a.R + s.rb * kRowsPerBlock + wq * 32) * kDv;
-        const int rows_left = a.R - (s.rb * kRowsPerBlock + wq * 32);  // rows of this warp inside the request
         if (mode == 1) {
           // fp16 partial O / l, scaled by a power of two that puts the row's
           // largest magnitude in [2^14, 2^15) (lse_part holds the scale): every
@@ -827,7 +945,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 v[32 + i] = __uint_as_float(o1[i]) * inv_l;
               }
             }
-            store_rows_bf16(est, v, dst, rows_left, cc, lane);
+            if (ring_free) {  // two 16 KB half boxes per warp, staged in the idle ring
+              uint8_t* hb = smem + (cc >> 2) * 65536 + wq * 16384;
+              stage_half(hb, v, cc & 3, lane);
+              if ((cc & 3) == 3) store_half(hb, &out_map4, cc >> 2, row0, s.b, a.R, lane);
+            } else {
+              store_rows_tma(est, v, &out_map, cc, row0, s.b, a.R, lane);
+            }
           }
           if (row_valid) a.lse[out_row] = lse_own;
         } else {
@@ -876,16 +1000,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           // is read from shared memory.  Otherwise it is read from global
           // memory directly.  With several other pieces, the running result
           // is kept in O (TMEM) between passes.
-          bool ring_free = true;
-          {
-            SegIter look = it;
-            Seg nx;
-            while (look.next(nx))
-              if (!nx.empty) {
-                ring_free = false;
-                break;
-              }
-          }
           const int own = c - c0;
           for (int pi = 0; pi < k - 1 && ok; ++pi) {
             const int i = pi < own ? pi : pi + 1;
@@ -937,8 +1051,15 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                   v[8 * q + 2 * h + 1] += cf * f2.y;
                 }
               }
-              if (last_pass) {
-                store_rows_bf16(est, v, dst, rows_left, cc, lane);
+              if (last_pass && ring_free) {
+                // half 0 staged in the ring's free top 64 KB; half 1 where the
+                // partial's chunks 0..31 were (read by every warp before it)
+                uint8_t* hb = (cc < 4 ? smem + 2 * 65536 : smem) + wq * 16384;
+                stage_half(hb, v, cc & 3, lane);
+                if ((cc & 3) == 3) store_half(hb, &out_map4, cc >> 2, row0, s.b, a.R, lane);
+                if (cc == 3 && !epi_sync()) { ok = false; break; }
+              } else if (last_pass) {
+                store_rows_tma(est, v, &out_map, cc, row0, s.b, a.R, lane);
               } else {
                 uint32_t o0[32], o1[32];
 #pragma unroll
@@ -971,6 +1092,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       }
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
+    if (!scorer && lane == 0) bulk_wait_all();  // output stores complete before the CTA ends
   } else if (warp == 6) {
     // ---------------------------------------------------------------- credit relay (accumulator)
     // After PV of tile t, P buffer t%2 may be refilled by the scorer; the
@@ -1126,13 +1248,14 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map9, const CUtensorMap& kv_map8,
+                          const CUtensorMap& q_map, const CUtensorMap& out_map, const CUtensorMap& out_map4,
                           int clusters, bool fp8, cudaStream_t stream) {
   cudaError_t e = set_smem_attr(fp8);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_cfg(fp8, clusters, stream, attr, true);
-  if (fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map9, kv_map8, a);
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map9, kv_map8, a);
+  if (fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map9, kv_map8, q_map, out_map, out_map4, a);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map9, kv_map8, q_map, out_map, out_map4, a);
 }
 
 }  // namespace mla_gb300

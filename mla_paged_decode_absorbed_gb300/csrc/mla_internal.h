@@ -64,7 +64,14 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters);
 // channel chunks, pages) with a chunk stride of 128 bytes; one box brings
 // chunks 0..8 (scorer) or 0..7 (accumulator) of a page, laid out in shared
 // memory as consecutive 64-token x 64-channel swizzled blocks.
+// q_map: q as a 4-D tensor (64 channels, 9 channel chunks, R rows, B) whose
+// box (64, 9, 64, 1) is half a row block (rows past R read as zeros).
+// out_map: out as a 3-D tensor (512 channels, R rows, B) whose box
+// (64, 32, 1) is 32 rows x 64 channels (rows past R are not written).
+// out_map4: out as a 4-D tensor (64 channels, R rows, 8 channel chunks, B)
+// whose box (64, 32, 4, 1) is 32 rows x 256 channels.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map9, const CUtensorMap& kv_map8,
+                          const CUtensorMap& q_map, const CUtensorMap& out_map, const CUtensorMap& out_map4,
                           int clusters, bool fp8, cudaStream_t stream);
 
 }  // namespace mla_gb300
