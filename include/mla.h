@@ -130,7 +130,7 @@ mla_status mla_plan(const mla_desc* desc, const int32_t* seqlens, void* workspac
  * plan of mla_plan() in the same workspace.  Writes out/lse for units that
  * were not split.  Every piece of a split unit writes a partial (normalised
  * output in fp16 with a power-of-two row scale, and its lse) into the
- * workspace; for a unit of at most four pieces the piece that finishes last
+ * workspace; for a unit of two or three pieces the piece that finishes last
  * merges the others' partials with its own result and writes out/lse itself.
  * Units of more pieces are left to mla_combine().  The kernel leaves the
  * workspace's merge counters clear, so it may run again on the same plan;
@@ -146,7 +146,7 @@ mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void*
 
 /*
  * Step 3 (LSE-weighted combine, one kernel): for every split unit of more
- * than four pieces,
+ * than three pieces,
  *   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
  * over its pieces, written to out (bf16) and lse.  Needs the plan and the
  * partials of the two previous steps in the same workspace; returns at once
@@ -192,11 +192,13 @@ const char* mla_status_string(int status);
 
 /* Byte offsets of the workspace regions (for tests and tools that inspect the
  * plan).  The header is int32 words: [0] error bits, [1] W, [2] total cost,
- * [3] units, [4] clusters, [5] plan overhead, [6] 1 if some unit has more than
- * four pieces (mla_combine() has work).  cl_first is int32 [clusters] (first
+ * [3] units, [4] clusters, [5] plan overhead, [6] number of units of more
+ * than three pieces (the combine jobs of mla_combine()).  cl_first is int32 [clusters] (first
  * unit each cluster touches), pre is int32 [units + 1] (cost prefix), sync is
- * int32 [3*clusters] (merge counters, then partial-slot ready flags; mla_plan()
- * clears them and every completed attention kernel leaves them clear),
+ * int32 [8*clusters]: merge counters [clusters] and partial-slot ready flags
+ * [2*clusters] (mla_plan() clears them and every completed attention kernel
+ * leaves them clear), then at [4*clusters] the combine jobs as int32 x 4
+ * (unit, first cluster, last cluster, slot of the first piece),
  * lse_part fp32 [2*clusters, 128, 2] (lse of the piece, power-of-two scale of
  * its stored output), o_part fp16 [2*clusters][64 chunks][128 rows][8] (slot
  * s, row r, channel ch at ((s*64 + ch/8)*128 + r)*8 + ch%8; the piece's

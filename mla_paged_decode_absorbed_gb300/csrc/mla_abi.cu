@@ -19,7 +19,7 @@ namespace mla_gb300 {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kCombineChunksPerCta = 2;  // 8-channel chunks of every row per combine CTA
+constexpr int kCombineChunksPerCta = 4;  // 8-channel chunks of every row per combine CTA
 constexpr int kCombineThreads = 128 * kCombineChunksPerCta;
 
 // ------------------------------------------------------------------ planner
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
                                                                 int32_t* hdr, int32_t* cl_first, int32_t* pre,
                                                                 int32_t* sync) {
   __shared__ int warp_sum[32];
-  __shared__ int s_W;
+  __shared__ int s_total, s_njobs;
   // the attention kernel may start its prologue now; it reads the plan only
   // after this grid has completed
   asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -57,16 +57,18 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
   const int lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     hdr[kHdrErr] = 0;
-    hdr[kHdrCombine] = 0;
+    s_njobs = 0;
   }
-  for (int i = tid; i < 3 * G; i += T) sync[i] = 0;
+  for (int i = tid; i < 4 * G; i += T) sync[i] = 0;
+  for (int c = tid; c < G; c += T) cl_first[c] = U;
   __syncthreads();
   int32_t* err = hdr + kHdrErr;
   const int chunk = (U + T - 1) / T;
   const int u0 = min(U, tid * chunk), u1 = min(U, u0 + chunk);
   int local = 0;
   for (int u = u0; u < u1; ++u) local += unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
-  // block-wide exclusive scan of `local`
+  // block-wide exclusive scan of `local` (everything after it stays on chip
+  // except the writes of the plan itself)
   int incl = local;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -85,37 +87,41 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
       if (lane >= d) vi += x;
     }
     if (lane < nw) warp_sum[lane] = vi - v;  // exclusive warp offsets
+    if (lane == nw - 1) s_total = vi;
   }
   __syncthreads();
-  int run = warp_sum[warp] + incl - local;
-  for (int u = u0; u < u1; ++u) {
-    pre[u] = run;
-    run += unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
-  }
-  if (u1 == U && u0 < u1) pre[U] = run;
-  if (U == 0 && tid == 0) pre[0] = 0;
-  __syncthreads();
+  const int total = s_total;
+  const int W = max(1, (total + G - 1) / G);
   if (tid == 0) {
-    const int total = pre[U];
-    const int W = max(1, (total + G - 1) / G);
-    s_W = W;
     hdr[kHdrW] = W;
     hdr[kHdrTotal] = total;
     hdr[kHdrUnits] = U;
     hdr[kHdrClusters] = G;
     hdr[kHdrOvh] = ovh;
+    pre[U] = total;
   }
-  for (int c = tid; c < G; c += T) cl_first[c] = U;
-  __syncthreads();
-  const int W = s_W;
-  bool many = false;
+  // combine jobs: units of more than kFuseMax pieces, as (unit, first cluster,
+  // last cluster, slot of the first piece); at most one per first cluster
+  int4* jobs = reinterpret_cast<int4*>(sync + 4 * G);
+  int run = warp_sum[warp] + incl - local;
   for (int u = u0; u < u1; ++u) {
-    const int p0 = pre[u], p1 = pre[u + 1];
+    const int p0 = run, p1 = run + unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
+    run = p1;
+    pre[u] = p0;
     const int cf = (p0 + W - 1) / W, cl = (p1 + W - 1) / W - 1;
     for (int c = cf; c <= cl && c < G; ++c) cl_first[c] = u;
-    if (p1 - p0 > ovh && (p1 - 1) / W - (p0 + ovh) / W + 1 > kFuseMax) many = true;
+    if (p1 - p0 > ovh) {
+      const int first = p0 + ovh, c0 = first / W, c1 = (p1 - 1) / W;
+      if (c1 - c0 + 1 > kFuseMax) {
+        const int j = atomicAdd(&s_njobs, 1);
+        jobs[j] = make_int4(u, c0, c1, first != c0 * W ? 2 * c0 + 1 : 2 * c0);
+      }
+    }
   }
-  if (many) atomicOr(hdr + kHdrCombine, 1);
+  __syncthreads();
+  const int njobs = s_njobs;
+  if (tid == 0) hdr[kHdrCombine] = njobs;
+  for (int j = njobs + tid; j < G; j += T) jobs[j] = make_int4(-1, 0, 0, 0);  // no job
 }
 
 // ------------------------------------------------------------------ combine
@@ -130,19 +136,10 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
   // launched as a programmatic dependent of the attention kernel: wait for it
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (a.hdr[kHdrCombine] == 0) return;  // nothing to do: every split unit was merged in place
-  const int c = blockIdx.x;
-  if (c + 1 >= a.clusters) return;
-  const int W = a.hdr[kHdrW];
-  const int u = a.cl_first[c + 1];
-  if (u >= a.U) return;
-  const int p0 = a.pre[u], p1 = a.pre[u + 1];
-  if (p1 - p0 - a.overhead <= 0) return;
-  const int first = p0 + a.overhead;
-  const int lo_c = c * W, hi_c = lo_c + W;
-  if (!(first >= lo_c && first < hi_c && p1 > hi_c)) return;
-  const int last = (p1 - 1) / W;
-  if (last - c + 1 <= kFuseMax) return;
+  // one CTA column per job (the planner marks unused job slots with unit -1)
+  const int4 job = reinterpret_cast<const int4*>(a.sync + 4 * a.clusters)[blockIdx.x];
+  if (job.x < 0) return;
+  const int u = job.x, c = job.y, last = job.z, slot0 = job.w;
   const int b = u % a.B, rb = u / a.B;
   const int L = threadIdx.x & (kRowsPerBlock - 1);                      // row within the block
   const int j = blockIdx.y * kCombineChunksPerCta + (threadIdx.x >> 7);  // 8-channel chunk
@@ -150,22 +147,39 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   if (r >= a.R) return;
   const float2* lp = reinterpret_cast<const float2*>(a.lse_part);
   const uint4* op = reinterpret_cast<const uint4*>(a.o_part);
-  auto slot_of = [&](int cc) { return (cc == c && first != lo_c) ? 2 * c + 1 : 2 * cc; };
-  float mx = -INFINITY;
-#pragma unroll 8
-  for (int cc = c; cc <= last; ++cc) mx = fmaxf(mx, lp[static_cast<size_t>(slot_of(cc)) * kRowsPerBlock + L].x);
+  // pieces in batches of 8 (all loads of a batch issued together), with a
+  // running max across batches
+  float mx = -INFINITY, wsum = 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float wsum = 0.f;
-  if (mx != -INFINITY) {
-#pragma unroll 8
-    for (int cc = c; cc <= last; ++cc) {
-      const int slot = slot_of(cc);
-      const float2 ls = lp[static_cast<size_t>(slot) * kRowsPerBlock + L];
-      const uint4 o = op[(static_cast<size_t>(slot) * kPartChunks + j) * kRowsPerBlock + L];
-      const float w = expf(ls.x - mx);  // 0 for a piece that saw no key of this row
+  for (int cb = c; cb <= last; cb += 8) {
+    float2 ls[8];
+    uint4 o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int cc = cb + i;
+      ls[i] = make_float2(-INFINITY, 0.f);
+      o[i] = make_uint4(0, 0, 0, 0);
+      if (cc <= last) {
+        const size_t slot = static_cast<size_t>(cc == c ? slot0 : 2 * cc);
+        ls[i] = lp[slot * kRowsPerBlock + L];
+        o[i] = op[(slot * kPartChunks + j) * kRowsPerBlock + L];
+      }
+    }
+    float bm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bm = fmaxf(bm, ls[i].x);
+    const float m_new = fmaxf(mx, bm);
+    if (m_new == -INFINITY) continue;  // no piece saw a key of this row yet
+    const float keep = mx == -INFINITY ? 0.f : expf(mx - m_new);
+    wsum *= keep;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) acc[h] *= keep;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = expf(ls[i].x - m_new);  // 0 for a piece that saw no key of this row
       wsum += w;
-      const float ws = w * ls.y;
-      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+      const float ws = w * ls[i].y;
+      const uint32_t ow[4] = {o[i].x, o[i].y, o[i].z, o[i].w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ow[h]));
@@ -173,6 +187,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
         acc[2 * h + 1] += ws * f.y;
       }
     }
+    mx = m_new;
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const size_t orow = static_cast<size_t>(b) * a.R + r;
@@ -232,7 +247,7 @@ mla_workspace_layout layout_for(const Dims& x, int G) {
   l.pre = off;
   off += align256(sizeof(int32_t) * (static_cast<size_t>(x.U) + 1));
   l.sync = off;
-  off += align256(sizeof(int32_t) * 3 * static_cast<size_t>(G));
+  off += align256(sizeof(int32_t) * 8 * static_cast<size_t>(G));
   l.lse_part = off;
   off += align256(sizeof(float) * 2 * 2 * static_cast<size_t>(G) * kRowsPerBlock);
   l.o_part = off;
@@ -458,6 +473,7 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   a.pre = reinterpret_cast<const int32_t*>(p.ws + p.lay.pre);
   a.o_part = p.ws + p.lay.o_part;
   a.lse_part = reinterpret_cast<const float*>(p.ws + p.lay.lse_part);
+  a.sync = reinterpret_cast<const int32_t*>(p.ws + p.lay.sync);
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.B = p.x.B;
@@ -467,7 +483,9 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   a.overhead = p.x.ovh;
   // programmatic dependent of the attention kernel (it waits on the device)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.G, kPartChunks / kCombineChunksPerCta, 1);
+  // a job unit has more than kFuseMax pieces, so it spans at least kFuseMax of
+  // the G - 1 cluster boundaries: there are at most (G - 1) / kFuseMax jobs
+  cfg.gridDim = dim3(p.G > kFuseMax ? (p.G - 1) / kFuseMax : 1, kPartChunks / kCombineChunksPerCta, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -15,7 +15,7 @@ constexpr int kDefaultOverhead = 2;  // planner cost per work unit, in pages
 // A split unit with at most this many pieces is merged inside the attention
 // kernel by the piece that finishes last; units with more pieces are merged by
 // the combine kernel.
-constexpr int kFuseMax = 4;
+constexpr int kFuseMax = 3;
 // Partial slots hold fp16 O / l in 8-channel chunks: [slot][kPartChunks][128 rows][8].
 constexpr int kPartChunks = 512 / 8;
 
@@ -23,7 +23,7 @@ constexpr int kPartChunks = 512 / 8;
 enum : int32_t { kErrBounds = 1, kErrTimeout = 2, kErrRange = 4 };
 
 // Workspace header words (int32).
-// kHdrCombine: 1 if some unit has more than kFuseMax pieces (the combine kernel has work).
+// kHdrCombine: number of units with more than kFuseMax pieces (combine jobs).
 enum : int { kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters = 4, kHdrOvh = 5, kHdrCombine = 6 };
 
 struct DecodeArgs {
@@ -51,6 +51,7 @@ struct CombineArgs {
   const int32_t* cl_first;
   const int32_t* pre;
   const void* o_part;
+  const int32_t* sync;        // merge counters, slot flags, then combine jobs (int4 at [4 * clusters])
   const float* lse_part;
   uint16_t* out;
   float* lse;
