@@ -1133,8 +1133,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       if (s.empty) continue;
       const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
       const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
+      const int dl = dq & 31;  // lane within this dequant warp
+      int ids = 0;             // page ids 32 at a time, one per lane
       for (int p = s.page_lo; p < s.page_hi; ++p) {
-        int pid = __ldg(bt + p);
+        if (((p - s.page_lo) & 31) == 0) {
+          const int pp = p + dl;
+          ids = pp < s.page_hi ? __ldg(bt + pp) : 0;
+        }
+        int pid = __shfl_sync(0xffffffffu, ids, (p - s.page_lo) & 31);
         bool bad = pid < 0 || pid >= a.num_pages;
         if (bad) {
           if (dq == 0) atomicOr(a.err, kErrBounds);
