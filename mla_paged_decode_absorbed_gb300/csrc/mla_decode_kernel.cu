@@ -31,8 +31,9 @@
 //   TMEM lane quarter each, one query row per thread) run the softmax
 //   (scorer) or the rescale and epilogue (accumulator); warp 6 of the
 //   accumulator returns P-buffer credits to the scorer.  The fp8-cache variant
-//   adds warps 7-10, which read e4m3 pages with plain coalesced loads and write
-//   fp16 into the ring (the MMAs then run in fp16).
+//   has the loader bulk-copy each page's e4m3 bytes into the top of its ring
+//   stage and adds warps 7-10, which rewrite the stage in place as fp16 (the
+//   MMAs then run in fp16).
 // * Online softmax in base 2 with a lazy rescale: the running max only moves
 //   (and O is only rescaled) when a tile's max exceeds it by more than 8 (a
 //   factor 256); the final division by the row sum is exact either way.  This
@@ -55,6 +56,7 @@ constexpr int kBox = 64 * 64 * 2;                  // 64 tokens x 64 channels, 1
 constexpr int kStages = 3;
 constexpr int kStageS = 9 * kBox;                  // scorer: channels 0..575
 constexpr int kStageO = 8 * kBox;                  // accumulator: channels 0..511
+constexpr int kRawPage = kPage * kDqk;             // fp8 cache: one page of e4m3 bytes
 constexpr int kPBytes = kRowsPerBlock * 64 * 2;    // P tile: 128 rows x 64 keys, SW128 K-major
 constexpr int kVecBytes = kRowsPerBlock * 4;       // one fp32 per row
 constexpr int kPartBytes = kPartChunks * kRowsPerBlock * 16;  // one fp16 partial slot (128 KB)
@@ -70,7 +72,7 @@ constexpr int kOffAlpha = kOffP + 2 * kPBytes;     // accumulator: rescale facto
 constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: (row sum, lse) [128]
 constexpr int kAccEnd = kOffL + kRowsPerBlock * 8;
 constexpr int kOffBars = kScorerEnd > kAccEnd ? kScorerEnd : kAccEnd;
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 320;
 constexpr int kSmemMax = 232448;
 constexpr int kSmem = kSmemMax;                    // layout + slack for aligning the base
 constexpr int kAlignSlack = kSmem - kOffBars - kBarBytes;
@@ -78,6 +80,7 @@ static_assert(kAlignSlack >= 0, "shared memory layout too large");
 
 // TMEM columns.  Scorer: Q (576 16-bit channels) then two S buffers.
 constexpr uint32_t kColQ = 0, kColS0 = 288, kColS1 = 352;
+
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -110,6 +113,8 @@ struct Bars {
   uint64_t epi_bar;       // accumulator: barrier of the four epilogue warps (128), bounded
                           // unlike bar.sync, so a warp that gives up cannot strand the others
   uint64_t drain;
+  uint64_t raw_full[kStages];  // fp8: the page's e4m3 bytes arrived in the stage (1 + tx)
+  uint64_t dq_sync;            // fp8: the dequant threads read the raw bytes (128), bounded
   int abort_flag;
   uint32_t tmem_base;
   int ticket;             // accumulator: finish order of this piece among its unit's pieces
@@ -306,6 +311,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(smem_u32(&bars->mrg_bar), 1);
     mbar_init(smem_u32(&bars->epi_bar), 128);
     mbar_init(smem_u32(&bars->drain), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars->raw_full[s]), 1);
+    mbar_init(smem_u32(&bars->dq_sync), 128);
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
@@ -376,7 +383,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t bytes = static_cast<uint32_t>(nbox * kBox);
     while (ok && it.next(s)) {
       if (s.empty) continue;
-      if (kFp8) continue;  // the fp8 variant's dequant warps read pages themselves
       const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
       for (int p0 = s.page_lo; ok && p0 < s.page_hi; p0 += 32) {
         const int my_p = p0 + lane;
@@ -405,12 +411,17 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             } else {
               if (pid < 0 || pid >= a.num_pages) {
                 atomicOr(a.err, kErrBounds);
-                pid = a.num_pages;  // outside the tensor map: TMA fills zeros, no fault
+                // bf16: outside the tensor map, TMA fills zeros.  fp8: page 0 is
+                // copied and the dequant warps write zeros for a bad id.
+                pid = kFp8 ? 0 : a.num_pages;
               }
-              const uint32_t fb = smem_u32(&bars->kv_full[stage]);
-              mbar_arrive_expect_tx(fb, bytes);
+              const uint32_t fb = smem_u32(kFp8 ? &bars->raw_full[stage] : &bars->kv_full[stage]);
+              mbar_arrive_expect_tx(fb, kFp8 ? static_cast<uint32_t>(kRawPage) : bytes);
               uint8_t* dst = smem + stage * stage_bytes;
-              if (scorer)
+              if (kFp8)
+                bulk_load(smem_u32(dst + stage_bytes - kRawPage),
+                          reinterpret_cast<const uint8_t*>(a.kv) + static_cast<size_t>(pid) * kRawPage, kRawPage, fb);
+              else if (scorer)
                 tma_load_4d(smem_u32(dst), &kv_map9, 0, 0, 0, pid, fb);
               else
                 tma_load_4d_hint(smem_u32(dst), &kv_map8, 0, 0, 0, pid, fb, policy);
@@ -437,7 +448,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     if (!ok && lane == 0) {
       // wait (time-bounded only) for the loads already in flight
       for (int i = 0; i < kStages; ++i)
-        if (last_par[i] >= 0) mbar_wait(smem_u32(&bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
+        if (last_par[i] >= 0)
+          mbar_wait(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
       if (q_tma_state >= 1) mbar_wait(smem_u32(&bars->q_tma), 0u, nullptr);
     }
     __syncwarp();
@@ -1118,83 +1130,94 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     __syncwarp();
   } else if (kFp8) {
     // ---------------------------------------------------------------- fp8 dequant (warps 7-10)
-    // e4m3 x scale -> fp16 in the ring, swizzled as the MMA descriptors expect;
-    // rows past seqlen are written as zeros.
-    const int dq = tid - 224;  // 0..127
-    const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(a.kv);
+    // The loader has bulk-copied the page's e4m3 bytes (64 rows of 576) into
+    // the top of the ring stage.  Each thread owns half of one token's
+    // channels: it reads its raw bytes into registers, all 128 threads meet at
+    // a (bounded) barrier because the fp16 rows overwrite the raw bytes, then it
+    // writes e4m3 x scale as fp16 in the layout the MMA descriptors expect.
+    // Rows past seqlen (and pages with a bad id) are written as zeros.
+    const int dq = tid - 224;                       // 0..127
+    const int t = dq >> 1, h = dq & 1;              // token in the page, half of its channels
+    const int nck = scorer ? 18 : 16;               // 16-channel chunks of this thread
+    const int ch0 = h * nck * 16;                   // first channel: 0, 288 (scorer) or 256
+    const int g0 = ch0 >> 7;                        // its scale group (0 or 2)
+    // chunk order rotated per thread so that the raw reads of a warp hit all banks
+    const int rot = scorer ? ((t >> 1) & 1) : 2 * h + ((t >> 1) & 1);
+    const uint32_t raw_off = static_cast<uint32_t>(stage_bytes - kRawPage);
     SegIter it = it0;
     Seg s;
     int stage = 0;
-    uint32_t ph = 0;
+    uint32_t ph = 0, sync_ph = 0;
     bool ok = true;
-    const int per_tok = nbox * 8;              // 16-byte output chunks per token
-    const int chunks = kPage * per_tok;        // per page
     while (ok && it.next(s)) {
       if (s.empty) continue;
       const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
       const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
-      const int dl = dq & 31;  // lane within this dequant warp
-      int ids = 0;             // page ids 32 at a time, one per lane
+      const int dl = dq & 31;
+      int ids = 0;  // page ids 32 at a time, one per lane
       for (int p = s.page_lo; p < s.page_hi; ++p) {
-        if (((p - s.page_lo) & 31) == 0) {
-          const int pp = p + dl;
-          ids = pp < s.page_hi ? __ldg(bt + pp) : 0;
+        const int slot = (p - s.page_lo) & 31;
+        if (slot == 0) ids = p + dl < s.page_hi ? __ldg(bt + p + dl) : 0;
+        int pid = __shfl_sync(0xffffffffu, ids, slot);
+        const bool bad = pid < 0 || pid >= a.num_pages;
+        if (bad && dq == 0) atomicOr(a.err, kErrBounds);
+        const bool live = !bad && t < seqlen - p * kPage;
+        // the scales are read while the page is still in flight
+        float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f;
+        if (live) {
+          const float* sp = a.kv_scales + (static_cast<size_t>(pid) * kPage + t) * kGroups + g0;
+          sc0 = __ldg(sp);
+          sc1 = __ldg(sp + 1);
+          if (scorer) sc2 = __ldg(sp + 2);
         }
-        int pid = __shfl_sync(0xffffffffu, ids, (p - s.page_lo) & 31);
-        bool bad = pid < 0 || pid >= a.num_pages;
-        if (bad) {
-          if (dq == 0) atomicOr(a.err, kErrBounds);
-          pid = 0;
+        if (!mbar_wait(smem_u32(&bars->raw_full[stage]), ph, abort_flag)) {
+          ok = false;
+          break;
         }
-        const int valid = bad ? 0 : seqlen - p * kPage;
-        uint8_t* dst = smem + stage * stage_bytes;
+        uint8_t* const dst = smem + stage * stage_bytes;
+        const uint8_t* const src = dst + raw_off + t * kDqk + ch0;
+        uint4 r[18];
+#pragma unroll
+        for (int j = 0; j < 18; ++j) {
+          int jj = j + rot;
+          if (jj >= nck) jj -= nck;
+          r[j] = make_uint4(0, 0, 0, 0);
+          if (live && j < nck) r[j] = *reinterpret_cast<const uint4*>(src + 16 * jj);
+        }
+        mbar_arrive(smem_u32(&bars->dq_sync));
+        if (!mbar_wait(smem_u32(&bars->dq_sync), sync_ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        sync_ph ^= 1u;
         bool out_of_range = false;
-        // two halves of up to 18 chunks per thread: loads of a half first, then
-        // conversion and stores (one 8-byte e4m3 group + its scale per chunk)
-        for (int half = 0; half < 2 && ok; ++half) {
-          uint2 raw[18];
-          float scl[18];
+        if (live) out_of_range = !(fmaxf(fabsf(sc0), fmaxf(fabsf(sc1), fabsf(sc2))) * 448.f <= 65504.f);
+        uint8_t* const row = dst + t * 128;
+        const int sw = t & 7;
 #pragma unroll
-          for (int i = 0; i < 18; ++i) {
-            const int q = dq + 128 * (18 * half + i);
-            raw[i] = make_uint2(0, 0);
-            scl[i] = 0.f;
-            if (q < chunks) {
-              const int tok = q / per_tok, rem = q - tok * per_tok;
-              if (tok < valid) {
-                const int ch = rem * 8;
-                const size_t row = static_cast<size_t>(pid) * kPage + tok;
-                raw[i] = __ldg(reinterpret_cast<const uint2*>(kv8 + row * kDqk + ch));
-                scl[i] = __ldg(a.kv_scales + row * kGroups + (ch < 512 ? (ch >> 7) : 4));
-              }
+        for (int j = 0; j < 18; ++j) {
+          if (j < nck) {
+            int jj = j + rot;
+            if (jj >= nck) jj -= nck;
+            const int c = ch0 + 16 * jj;
+            const int gk = (c < 512 ? (c >> 7) : 4) - g0;
+            const float sv = gk == 0 ? sc0 : (gk == 1 ? sc1 : sc2);
+            const uint32_t wd[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float f0, f1, f2, f3;
+              e4m3x2_to_f32(static_cast<uint16_t>(wd[k] & 0xFFFFu), f0, f1);
+              e4m3x2_to_f32(static_cast<uint16_t>(wd[k] >> 16), f2, f3);
+              o[2 * k] = pack_f16x2(f0 * sv, f1 * sv);
+              o[2 * k + 1] = pack_f16x2(f2 * sv, f3 * sv);
             }
-          }
-          if (half == 0 && !mbar_wait(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int i = 0; i < 18; ++i) {
-            const int q = dq + 128 * (18 * half + i);
-            if (q >= chunks) break;
-            const int tok = q / per_tok, rem = q - tok * per_tok;
-            const int box = rem >> 3, c8 = rem & 7;
-            const float sv = scl[i];
-            out_of_range |= !(fabsf(sv) * 448.f <= 65504.f);
-            float f[8];
-            e4m3x2_to_f32(static_cast<uint16_t>(raw[i].x & 0xFFFFu), f[0], f[1]);
-            e4m3x2_to_f32(static_cast<uint16_t>(raw[i].x >> 16), f[2], f[3]);
-            e4m3x2_to_f32(static_cast<uint16_t>(raw[i].y & 0xFFFFu), f[4], f[5]);
-            e4m3x2_to_f32(static_cast<uint16_t>(raw[i].y >> 16), f[6], f[7]);
-            uint4 w;
-            w.x = pack_f16x2(f[0] * sv, f[1] * sv);
-            w.y = pack_f16x2(f[2] * sv, f[3] * sv);
-            w.z = pack_f16x2(f[4] * sv, f[5] * sv);
-            w.w = pack_f16x2(f[6] * sv, f[7] * sv);
-            *reinterpret_cast<uint4*>(dst + box * kBox + tok * 128 + ((c8 ^ (tok & 7)) << 4)) = w;
+            const int c8 = (c & 63) >> 3;
+            uint8_t* const bx = row + (c >> 6) * kBox;
+            *reinterpret_cast<uint4*>(bx + ((c8 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(bx + (((c8 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
-        if (!ok) break;
         if (out_of_range) atomicOr(a.err, kErrRange);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&bars->kv_full[stage]));
