@@ -248,14 +248,15 @@ __device__ __forceinline__ void store_half(uint8_t* half_buf, const CUtensorMap*
   __syncwarp();
 }
 
-// e4m3 x2 -> two floats (exact through f16).
-__device__ __forceinline__ void e4m3x2_to_f32(uint16_t v, float& lo, float& hi) {
+// e4m3 x2 times a scale given as hi + lo halves (hi = fp16(scale), lo =
+// fp16(scale - hi)) -> f16x2.  x*lo is small, so the fused x*hi + x*lo is
+// rounded once: within a tiny error of fp16(x * scale) for scales >= 2^-14.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint16_t v, __half2 hi, __half2 lo) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  float2 f = __half22float2(h);
-  lo = f.x;
-  hi = f.y;
+  const __half2 x = *reinterpret_cast<const __half2*>(&h2);
+  const __half2 y = __hfma2(x, hi, __hmul2(x, lo));
+  return *reinterpret_cast<const uint32_t*>(&y);
 }
 
 // Tree reductions over 64 values (independent chains for ILP).
@@ -1192,6 +1193,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         sync_ph ^= 1u;
         bool out_of_range = false;
         if (live) out_of_range = !(fmaxf(fabsf(sc0), fmaxf(fabsf(sc1), fabsf(sc2))) * 448.f <= 65504.f);
+        const __half hi0 = __float2half_rn(sc0), hi1 = __float2half_rn(sc1), hi2 = __float2half_rn(sc2);
+        const __half lo0 = __float2half_rn(sc0 - __half2float(hi0)), lo1 = __float2half_rn(sc1 - __half2float(hi1)),
+                     lo2 = __float2half_rn(sc2 - __half2float(hi2));
         uint8_t* const row = dst + t * 128;
         const int sw = t & 7;
 #pragma unroll
@@ -1201,16 +1205,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (jj >= nck) jj -= nck;
             const int c = ch0 + 16 * jj;
             const int gk = (c < 512 ? (c >> 7) : 4) - g0;
-            const float sv = gk == 0 ? sc0 : (gk == 1 ? sc1 : sc2);
+            const __half2 shi = __half2half2(gk == 0 ? hi0 : (gk == 1 ? hi1 : hi2));
+            const __half2 slo = __half2half2(gk == 0 ? lo0 : (gk == 1 ? lo1 : lo2));
             const uint32_t wd[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
             uint32_t o[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              float f0, f1, f2, f3;
-              e4m3x2_to_f32(static_cast<uint16_t>(wd[k] & 0xFFFFu), f0, f1);
-              e4m3x2_to_f32(static_cast<uint16_t>(wd[k] >> 16), f2, f3);
-              o[2 * k] = pack_f16x2(f0 * sv, f1 * sv);
-              o[2 * k + 1] = pack_f16x2(f2 * sv, f3 * sv);
+              o[2 * k] = e4m3x2_scaled_f16x2(static_cast<uint16_t>(wd[k] & 0xFFFFu), shi, slo);
+              o[2 * k + 1] = e4m3x2_scaled_f16x2(static_cast<uint16_t>(wd[k] >> 16), shi, slo);
             }
             const int c8 = (c & 63) >> 3;
             uint8_t* const bx = row + (c >> 6) * kBox;
