@@ -29,11 +29,11 @@
 // * Roles per CTA: warp 0 loads pages (TMA, 32 block-table entries per read);
 //   warp 1 allocates TMEM and issues the MMAs from one lane; warps 2-5 (one
 //   TMEM lane quarter each, one query row per thread) run the softmax
-//   (scorer) or the rescale and epilogue (accumulator); warp 6 of the
-//   accumulator returns P-buffer credits to the scorer.  The fp8-cache variant
-//   has the loader bulk-copy each page's e4m3 bytes into the top of its ring
-//   stage and adds warps 7-10, which rewrite the stage in place as fp16 (the
-//   MMAs then run in fp16).
+//   (scorer) or the rescale and epilogue (accumulator).  The accumulator's PV
+//   commit multicasts the P-buffer credit straight to the scorer's barrier.
+//   The fp8-cache variant has the loader bulk-copy each page's e4m3 bytes into
+//   the top of its ring stage and adds warps 6-9, which rewrite the stage in
+//   place as fp16 (the MMAs then run in fp16).
 // * Online softmax in base 2 with a lazy rescale: the running max only moves
 //   (and O is only rescaled) when a tile's max exceeds it by more than 8 (a
 //   factor 256); the final division by the row sum is exact either way.  This
@@ -88,7 +88,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kThreads = kFp8 ? 352 : 224;
+  static constexpr int kThreads = kFp8 ? 320 : 192;
 };
 
 struct Bars {
@@ -524,6 +524,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                        (j > s.page_lo || k > 0) ? 1u : 0u);
             mma_commit(smem_u32(&bars->kv_empty[stage]));
             mma_commit(smem_u32(&bars->pv_done[sb]));
+            // P buffer sb may be refilled by the scorer once this PV is done; the
+            // buffer of a segment's last tile is returned by the epilogue instead,
+            // which stages its stores there.
+            if (j + 1 < s.page_hi) mma_commit_multicast(smem_u32(&bars->pbuf_free[sb]), static_cast<uint16_t>(1u << peer));
             if (j + 1 == s.page_hi) mma_commit(smem_u32(&bars->o_full));
           }
           __syncwarp();
@@ -1106,44 +1110,23 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
     if (!scorer && lane == 0) bulk_wait_all();  // output stores complete before the CTA ends
-  } else if (warp == 6) {
-    // ---------------------------------------------------------------- credit relay (accumulator)
-    // After PV of tile t, P buffer t%2 may be refilled by the scorer; the
-    // buffer of a segment's last tile is returned by the epilogue instead,
-    // which stages its stores there.
-    if (!scorer && lane == 0) {
-      const uint32_t rFree0 = mapa_shared(smem_u32(&bars->pbuf_free[0]), peer);
-      const uint32_t rFree1 = mapa_shared(smem_u32(&bars->pbuf_free[1]), peer);
-      SegIter it = it0;
-      Seg s;
-      uint32_t t = 0;
-      bool ok = true;
-      while (ok && it.next(s)) {
-        if (s.empty) continue;
-        for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
-          const uint32_t sb = t & 1u;
-          if (!mbar_wait(smem_u32(&bars->pv_done[sb]), (t >> 1) & 1u, abort_flag)) { ok = false; break; }
-          if (j + 1 < s.page_hi) mbar_arrive_remote(sb ? rFree1 : rFree0);
-        }
-      }
-      if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
-    }
-    __syncwarp();
   } else if (kFp8) {
-    // ---------------------------------------------------------------- fp8 dequant (warps 7-10)
+    // ---------------------------------------------------------------- fp8 dequant (warps 6-9)
     // The loader has bulk-copied the page's e4m3 bytes (64 rows of 576) into
     // the top of the ring stage.  Each thread owns half of one token's
     // channels: it reads its raw bytes into registers, all 128 threads meet at
     // a (bounded) barrier because the fp16 rows overwrite the raw bytes, then it
     // writes e4m3 x scale as fp16 in the layout the MMA descriptors expect.
     // Rows past seqlen (and pages with a bad id) are written as zeros.
-    const int dq = tid - 224;                       // 0..127
+    const int dq = tid - 192;                       // 0..127
     const int t = dq >> 1, h = dq & 1;              // token in the page, half of its channels
     const int nck = scorer ? 18 : 16;               // 16-channel chunks of this thread
     const int ch0 = h * nck * 16;                   // first channel: 0, 288 (scorer) or 256
     const int g0 = ch0 >> 7;                        // its scale group (0 or 2)
-    // chunk order rotated per thread so that the raw reads of a warp hit all banks
-    const int rot = scorer ? ((t >> 1) & 1) : 2 * h + ((t >> 1) & 1);
+    // Chunk order rotated per thread so that both the raw reads and the
+    // swizzled 16-byte fp16 writes of a warp spread over all eight bank groups
+    // (four wavefronts per warp access, the minimum).
+    const int rot = scorer ? ((t >> 2) & 1) : 2 * ((t >> 1) & 1) + h;
     const uint32_t raw_off = static_cast<uint32_t>(stage_bytes - kRawPage);
     SegIter it = it0;
     Seg s;
