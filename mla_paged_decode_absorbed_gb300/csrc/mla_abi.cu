@@ -324,6 +324,25 @@ mla_status make_kv_map4(const void* kv, int num_pages, int chunks, CUtensorMap* 
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
+// fp8 cache [P, 64, 576] e4m3 as a 4-D byte tensor (64 bytes, 64 tokens, 9
+// chunks of 64 channels, pages): box (64, 64, `chunks`, 1) brings `chunks`
+// consecutive 64-channel chunks of a page as 64-token x 64-byte slots,
+// 64-byte swizzled (so that both the dequant reads and its swizzled 16-byte
+// fp16 writes are free of bank conflicts).
+mla_status make_kv_map_fp8(const void* kv, int num_pages, int chunks, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(kPage), 9, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {kDqk, 64, static_cast<cuuint64_t>(kDqk) * kPage};
+  cuuint32_t box[4] = {64, 64, static_cast<cuuint32_t>(chunks), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
 // q [B, R, 576] bf16 as a 4-D tensor (64 channels, 9 chunks, R rows, B): one
 // box (64, 9, 64, 1) is half a 128-row block (72 KB), 128-byte swizzled; rows
 // past R read as zeros.
@@ -423,13 +442,21 @@ mla_status run_plan(const Prepared& p, const int32_t* seqlens, cudaStream_t stre
 mla_status run_attention(const Prepared& p, const void* q, const void* kv, const float* kv_scales,
                          const int32_t* bt, const int32_t* seqlens, float scale, void* out, float* lse,
                          cudaStream_t stream) {
-  // the fp8 variant reads pages with plain loads and uses neither map
-  CUtensorMap map9, map8;
-  std::memset(&map9, 0, sizeof(map9));
-  std::memset(&map8, 0, sizeof(map8));
-  if (!p.x.fp8) {
-    mla_status st = make_kv_map4(kv, p.x.P, 9, &map9);
-    if (st == MLA_OK) st = make_kv_map4(kv, p.x.P, 8, &map8);
+  // page maps of the scorer and the accumulator: bf16, 9 and 8 swizzled
+  // 64-channel blocks; fp8, raw e4m3 chunks [0, kFp8ScorerBlocks) and
+  // [kFp8ScorerBlocks, 8), plus the RoPE chunk for the scorer
+  CUtensorMap map_s, map_a, map_r;
+  std::memset(&map_r, 0, sizeof(map_r));
+  {
+    mla_status st;
+    if (p.x.fp8) {
+      st = make_kv_map_fp8(kv, p.x.P, kFp8ScorerBlocks, &map_s);
+      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, 8 - kFp8ScorerBlocks, &map_a);
+      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, 1, &map_r);
+    } else {
+      st = make_kv_map4(kv, p.x.P, 9, &map_s);
+      if (st == MLA_OK) st = make_kv_map4(kv, p.x.P, 8, &map_a);
+    }
     if (st != MLA_OK) return st;
   }
   CUtensorMap qmap, omap, omap4;
@@ -463,7 +490,7 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   a.max_pages = p.x.maxp;
   a.overhead = p.x.ovh;
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_status(launch_decode(a, map9, map8, qmap, omap, omap4, p.G, p.x.fp8, stream));
+  return launch_status(launch_decode(a, map_s, map_a, map_r, qmap, omap, omap4, p.G, p.x.fp8, stream));
 }
 
 mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t stream) {

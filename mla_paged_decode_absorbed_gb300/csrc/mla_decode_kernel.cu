@@ -56,7 +56,19 @@ constexpr int kBox = 64 * 64 * 2;                  // 64 tokens x 64 channels, 1
 constexpr int kStages = 3;
 constexpr int kStageS = 9 * kBox;                  // scorer: channels 0..575
 constexpr int kStageO = 8 * kBox;                  // accumulator: channels 0..511
-constexpr int kRawPage = kPage * kDqk;             // fp8 cache: one page of e4m3 bytes
+// fp8 cache: the scorer converts latent blocks [0, kSB) and the RoPE block,
+// the accumulator latent blocks [kSB, 8); each copies its latent blocks into
+// the other's ring stage.  A CTA's raw e4m3 chunks (64 tokens x 64 bytes each,
+// 64-byte swizzled) sit in the part of its stage that the other's copy fills.
+constexpr int kSB = kFp8ScorerBlocks;
+constexpr int kRawSlot = 64 * 64;                  // one raw chunk: 64 tokens x 64 bytes
+constexpr int kRawOffS = kSB * kBox;               // scorer: raw chunks 0..kSB-1, then the RoPE chunk
+constexpr int kRawOffA = 0;                        // accumulator: raw chunks kSB..7
+constexpr int kRawBytesS = (kSB + 1) * kRawSlot;
+constexpr int kRawBytesA = (8 - kSB) * kRawSlot;
+static_assert(kRawOffS + kRawBytesS <= 8 * kBox && kRawOffA + kRawBytesA <= kSB * kBox,
+              "raw chunks must lie in the region the peer's copy fills");
+static_assert(2 * (kSB + 1) <= 10 && 2 * (8 - kSB) <= 10, "at most 10 pieces per dequant thread");
 constexpr int kPBytes = kRowsPerBlock * 64 * 2;    // P tile: 128 rows x 64 keys, SW128 K-major
 constexpr int kVecBytes = kRowsPerBlock * 4;       // one fp32 per row
 constexpr int kPartBytes = kPartChunks * kRowsPerBlock * 16;  // one fp16 partial slot (128 KB)
@@ -113,8 +125,10 @@ struct Bars {
   uint64_t epi_bar;       // accumulator: barrier of the four epilogue warps (128), bounded
                           // unlike bar.sync, so a warp that gives up cannot strand the others
   uint64_t drain;
-  uint64_t raw_full[kStages];  // fp8: the page's e4m3 bytes arrived in the stage (1 + tx)
-  uint64_t dq_sync;            // fp8: the dequant threads read the raw bytes (128), bounded
+  uint64_t raw_full[kStages];    // fp8: this CTA's raw e4m3 chunks arrived (1 + tx)
+  uint64_t dq_sync;              // fp8: the dequant threads wrote their blocks (128), bounded
+  uint64_t peer_empty[kStages];  // fp8: the peer's MMAs finished the stage (peer's multicast commit)
+  uint64_t raw_free[kStages];    // fp8: the peer read its raw chunks, our copy may land (remote, 1)
   int abort_flag;
   uint32_t tmem_base;
   int ticket;             // accumulator: finish order of this piece among its unit's pieces
@@ -270,7 +284,8 @@ __device__ __forceinline__ float max64(const float (&x)[64]) {
 
 template <bool kFp8>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map9, const __grid_constant__ CUtensorMap kv_map8,
+    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map_s, const __grid_constant__ CUtensorMap kv_map_a,
+                      const __grid_constant__ CUtensorMap kv_map_r,
                       const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap out_map,
                       const __grid_constant__ CUtensorMap out_map4, const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -290,7 +305,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->kv_full[s]), kFp8 ? 128 : 1);
+      // fp8: 128 dequant threads + the loader's expect_tx for the peer's copy
+      mbar_init(smem_u32(&bars->kv_full[s]), kFp8 ? 129 : 1);
       mbar_init(smem_u32(&bars->kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars->q_full), 128);
@@ -312,13 +328,18 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(smem_u32(&bars->mrg_bar), 1);
     mbar_init(smem_u32(&bars->epi_bar), 128);
     mbar_init(smem_u32(&bars->drain), 1);
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars->raw_full[s]), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->raw_full[s]), 1);
+      mbar_init(smem_u32(&bars->peer_empty[s]), 1);
+      mbar_init(smem_u32(&bars->raw_free[s]), 1);
+    }
     mbar_init(smem_u32(&bars->dq_sync), 128);
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
   }
   if (warp == 0 && lane == 0) {
-    if (!kFp8) tma_prefetch_desc(scorer ? &kv_map9 : &kv_map8);
+    tma_prefetch_desc(scorer ? &kv_map_s : &kv_map_a);
+    if (kFp8 && scorer) tma_prefetch_desc(&kv_map_r);
     if (!kFp8 && scorer) tma_prefetch_desc(&q_map);
     if (!scorer) {
       tma_prefetch_desc(&out_map);
@@ -412,20 +433,28 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             } else {
               if (pid < 0 || pid >= a.num_pages) {
                 atomicOr(a.err, kErrBounds);
-                // bf16: outside the tensor map, TMA fills zeros.  fp8: page 0 is
-                // copied and the dequant warps write zeros for a bad id.
-                pid = kFp8 ? 0 : a.num_pages;
+                pid = a.num_pages;  // outside the tensor map: TMA fills zeros, no fault
               }
               const uint32_t fb = smem_u32(kFp8 ? &bars->raw_full[stage] : &bars->kv_full[stage]);
-              mbar_arrive_expect_tx(fb, kFp8 ? static_cast<uint32_t>(kRawPage) : bytes);
               uint8_t* dst = smem + stage * stage_bytes;
-              if (kFp8)
-                bulk_load(smem_u32(dst + stage_bytes - kRawPage),
-                          reinterpret_cast<const uint8_t*>(a.kv) + static_cast<size_t>(pid) * kRawPage, kRawPage, fb);
-              else if (scorer)
-                tma_load_4d(smem_u32(dst), &kv_map9, 0, 0, 0, pid, fb);
-              else
-                tma_load_4d_hint(smem_u32(dst), &kv_map8, 0, 0, 0, pid, fb, policy);
+              if (kFp8) {
+                // the peer's converted blocks will complete on kv_full
+                mbar_arrive_expect_tx(smem_u32(&bars->kv_full[stage]),
+                                      static_cast<uint32_t>(scorer ? (8 - kSB) * kBox : kSB * kBox));
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(scorer ? kRawBytesS : kRawBytesA));
+                if (scorer) {
+                  tma_load_4d(smem_u32(dst + kRawOffS), &kv_map_s, 0, 0, 0, pid, fb);
+                  tma_load_4d(smem_u32(dst + kRawOffS + kSB * kRawSlot), &kv_map_r, 0, 0, 8, pid, fb);
+                } else {
+                  tma_load_4d(smem_u32(dst + kRawOffA), &kv_map_a, 0, 0, kSB, pid, fb);
+                }
+              } else if (scorer) {
+                mbar_arrive_expect_tx(fb, bytes);
+                tma_load_4d(smem_u32(dst), &kv_map_s, 0, 0, 0, pid, fb);
+              } else {
+                mbar_arrive_expect_tx(fb, bytes);
+                tma_load_4d_hint(smem_u32(dst), &kv_map_a, 0, 0, 0, pid, fb, policy);
+              }
               last_par[stage] = static_cast<int>(ph);
               if (q_tma_state == 0) {
                 q_tma_state = 1;
@@ -483,6 +512,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                      idesc, k > 0 ? 1u : 0u);
             mma_commit(smem_u32(&bars->s_full[sb]));
             mma_commit(smem_u32(&bars->kv_empty[stage]));
+            if (kFp8) mma_commit_multicast(smem_u32(&bars->peer_empty[stage]), static_cast<uint16_t>(1u << peer));
           }
           __syncwarp();
           if (++stage == kStages) {
@@ -523,6 +553,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                        vb + static_cast<uint64_t>((h * 4 * kBox + k * 2048) >> 4), idesc,
                        (j > s.page_lo || k > 0) ? 1u : 0u);
             mma_commit(smem_u32(&bars->kv_empty[stage]));
+            if (kFp8) mma_commit_multicast(smem_u32(&bars->peer_empty[stage]), static_cast<uint16_t>(1u << peer));
             mma_commit(smem_u32(&bars->pv_done[sb]));
             // P buffer sb may be refilled by the scorer once this PV is done; the
             // buffer of a segment's last tile is returned by the epilogue instead,
@@ -1112,27 +1143,35 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     if (!scorer && lane == 0) bulk_wait_all();  // output stores complete before the CTA ends
   } else if (kFp8) {
     // ---------------------------------------------------------------- fp8 dequant (warps 6-9)
-    // The loader has bulk-copied the page's e4m3 bytes (64 rows of 576) into
-    // the top of the ring stage.  Each thread owns half of one token's
-    // channels: it reads its raw bytes into registers, all 128 threads meet at
-    // a (bounded) barrier because the fp16 rows overwrite the raw bytes, then it
-    // writes e4m3 x scale as fp16 in the layout the MMA descriptors expect.
-    // Rows past seqlen (and pages with a bad id) are written as zeros.
+    // This CTA's raw chunks (64-byte swizzled) -> e4m3 x scale as fp16 in its
+    // own latent blocks (scorer: [0, kSB) and the RoPE block; accumulator:
+    // [kSB, 8)), 128-byte swizzled as the MMA descriptors expect.  Thread =
+    // (token t = lane-major, half h); each converts n 16-channel pieces.  Then
+    // one thread copies the latent blocks into the peer's stage once the peer
+    // has read its raw chunks there.  Rows past seqlen (and pages with a bad
+    // id, which TMA reads as zeros) are written as zeros.
     const int dq = tid - 192;                       // 0..127
-    const int t = dq >> 1, h = dq & 1;              // token in the page, half of its channels
-    const int nck = scorer ? 18 : 16;               // 16-channel chunks of this thread
-    const int ch0 = h * nck * 16;                   // first channel: 0, 288 (scorer) or 256
-    const int g0 = ch0 >> 7;                        // its scale group (0 or 2)
-    // Chunk order rotated per thread so that both the raw reads and the
-    // swizzled 16-byte fp16 writes of a warp spread over all eight bank groups
-    // (four wavefronts per warp access, the minimum).
-    const int rot = scorer ? ((t >> 2) & 1) : 2 * ((t >> 1) & 1) + h;
-    const uint32_t raw_off = static_cast<uint32_t>(stage_bytes - kRawPage);
+    const int t = dq & 63, h = dq >> 6;
+    const int n = scorer ? 2 * (kSB + 1) : 2 * (8 - kSB);  // 16-channel pieces per thread
+    // piece f of a token: raw slot f >> 2, quarter f & 3; its channel
+    auto piece_ch = [&](int f) -> int {
+      const int slot = f >> 2;
+      const int chunk = scorer ? (slot < kSB ? slot : 8) : kSB + slot;
+      return 64 * chunk + 16 * (f & 3);
+    };
+    auto group_of = [](int c) -> int { return c < 512 ? (c >> 7) : 4; };
+    const int g_lo = group_of(piece_ch(n * h)), g_hi = group_of(piece_ch(n * h + n - 1));
+    const uint32_t raw_off = static_cast<uint32_t>(scorer ? kRawOffS : kRawOffA);
+    // latent blocks this CTA sends, at the same offsets in the peer's stage
+    const uint32_t send_off = static_cast<uint32_t>(scorer ? 0 : kSB * kBox);
+    const uint32_t send_bytes = static_cast<uint32_t>(scorer ? kSB * kBox : (8 - kSB) * kBox);
+    const int peer_stage_bytes = scorer ? kStageO : kStageS;
+    const uint32_t peer_smem = mapa_shared(smem_u32(smem), peer);
     SegIter it = it0;
     Seg s;
     int stage = 0;
     uint32_t ph = 0, sync_ph = 0;
-    bool ok = true;
+    bool ok = true, sent_any = false;
     while (ok && it.next(s)) {
       if (s.empty) continue;
       const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
@@ -1142,70 +1181,79 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       for (int p = s.page_lo; p < s.page_hi; ++p) {
         const int slot = (p - s.page_lo) & 31;
         if (slot == 0) ids = p + dl < s.page_hi ? __ldg(bt + p + dl) : 0;
-        int pid = __shfl_sync(0xffffffffu, ids, slot);
-        const bool bad = pid < 0 || pid >= a.num_pages;
-        if (bad && dq == 0) atomicOr(a.err, kErrBounds);
+        const int pid = __shfl_sync(0xffffffffu, ids, slot);
+        const bool bad = pid < 0 || pid >= a.num_pages;  // the loader reports it
         const bool live = !bad && t < seqlen - p * kPage;
-        // the scales are read while the page is still in flight
-        float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f;
+        float s_lo = 0.f, s_hi = 0.f;
         if (live) {
-          const float* sp = a.kv_scales + (static_cast<size_t>(pid) * kPage + t) * kGroups + g0;
-          sc0 = __ldg(sp);
-          sc1 = __ldg(sp + 1);
-          if (scorer) sc2 = __ldg(sp + 2);
+          const float* sp = a.kv_scales + (static_cast<size_t>(pid) * kPage + t) * kGroups;
+          s_lo = __ldg(sp + g_lo);
+          s_hi = __ldg(sp + g_hi);
+        }
+        // our blocks of this stage were copied to the peer three pages ago:
+        // reuse them only after the peer's MMAs are done with that page
+        if (!mbar_wait<true>(smem_u32(&bars->peer_empty[stage]), ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
         }
         if (!mbar_wait(smem_u32(&bars->raw_full[stage]), ph, abort_flag)) {
           ok = false;
           break;
         }
+        const bool out_of_range = live && !(fmaxf(fabsf(s_lo), fabsf(s_hi)) * 448.f <= 65504.f);
+        const __half hl = __float2half_rn(s_lo), hh = __float2half_rn(s_hi);
+        const __half ll = __float2half_rn(s_lo - __half2float(hl)), lh = __float2half_rn(s_hi - __half2float(hh));
         uint8_t* const dst = smem + stage * stage_bytes;
-        const uint8_t* const src = dst + raw_off + t * kDqk + ch0;
-        uint4 r[18];
+        const uint8_t* const raw = dst + raw_off + t * 64;
+        const int sw = t & 7, rsw = (t >> 1) & 3;
 #pragma unroll
-        for (int j = 0; j < 18; ++j) {
-          int jj = j + rot;
-          if (jj >= nck) jj -= nck;
-          r[j] = make_uint4(0, 0, 0, 0);
-          if (live && j < nck) r[j] = *reinterpret_cast<const uint4*>(src + 16 * jj);
+        for (int i = 0; i < 10; ++i) {
+          if (i < n) {
+            const int f = n * h + i;
+            const int c = piece_ch(f);
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (live) {
+              const uint4 r = *reinterpret_cast<const uint4*>(raw + (f >> 2) * kRawSlot + (((f & 3) ^ rsw) << 4));
+              const bool lo = group_of(c) == g_lo;
+              const __half2 shi = __half2half2(lo ? hl : hh), slo = __half2half2(lo ? ll : lh);
+              o0.x = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.x & 0xFFFFu), shi, slo);
+              o0.y = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.x >> 16), shi, slo);
+              o0.z = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.y & 0xFFFFu), shi, slo);
+              o0.w = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.y >> 16), shi, slo);
+              o1.x = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.z & 0xFFFFu), shi, slo);
+              o1.y = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.z >> 16), shi, slo);
+              o1.z = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.w & 0xFFFFu), shi, slo);
+              o1.w = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.w >> 16), shi, slo);
+            }
+            const int c8 = (c & 63) >> 3;
+            uint8_t* const row = dst + (c >> 6) * kBox + t * 128;
+            *reinterpret_cast<uint4*>(row + ((c8 ^ sw) << 4)) = o0;
+            *reinterpret_cast<uint4*>(row + (((c8 + 1) ^ sw) << 4)) = o1;
+          }
         }
+        if (out_of_range) atomicOr(a.err, kErrRange);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bars->kv_full[stage]));
         mbar_arrive(smem_u32(&bars->dq_sync));
         if (!mbar_wait(smem_u32(&bars->dq_sync), sync_ph, abort_flag)) {
           ok = false;
           break;
         }
         sync_ph ^= 1u;
-        bool out_of_range = false;
-        if (live) out_of_range = !(fmaxf(fabsf(sc0), fmaxf(fabsf(sc1), fabsf(sc2))) * 448.f <= 65504.f);
-        const __half hi0 = __float2half_rn(sc0), hi1 = __float2half_rn(sc1), hi2 = __float2half_rn(sc2);
-        const __half lo0 = __float2half_rn(sc0 - __half2float(hi0)), lo1 = __float2half_rn(sc1 - __half2float(hi1)),
-                     lo2 = __float2half_rn(sc2 - __half2float(hi2));
-        uint8_t* const row = dst + t * 128;
-        const int sw = t & 7;
-#pragma unroll
-        for (int j = 0; j < 18; ++j) {
-          if (j < nck) {
-            int jj = j + rot;
-            if (jj >= nck) jj -= nck;
-            const int c = ch0 + 16 * jj;
-            const int gk = (c < 512 ? (c >> 7) : 4) - g0;
-            const __half2 shi = __half2half2(gk == 0 ? hi0 : (gk == 1 ? hi1 : hi2));
-            const __half2 slo = __half2half2(gk == 0 ? lo0 : (gk == 1 ? lo1 : lo2));
-            const uint32_t wd[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
-            uint32_t o[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              o[2 * k] = e4m3x2_scaled_f16x2(static_cast<uint16_t>(wd[k] & 0xFFFFu), shi, slo);
-              o[2 * k + 1] = e4m3x2_scaled_f16x2(static_cast<uint16_t>(wd[k] >> 16), shi, slo);
-            }
-            const int c8 = (c & 63) >> 3;
-            uint8_t* const bx = row + (c >> 6) * kBox;
-            *reinterpret_cast<uint4*>(bx + ((c8 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(bx + (((c8 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        if (dq == 0) {
+          // our raw chunks are read: the peer's copy may land on them
+          mbar_arrive_remote(mapa_shared(smem_u32(&bars->raw_free[stage]), peer));
+          if (!mbar_wait<true>(smem_u32(&bars->raw_free[stage]), ph, abort_flag)) {
+            ok = false;
+          } else {
+            const uint32_t poff = static_cast<uint32_t>(stage * peer_stage_bytes) + send_off;
+            bulk_copy_peer(peer_smem + poff, smem_u32(dst + send_off), send_bytes,
+                           mapa_shared(smem_u32(&bars->kv_full[stage]), peer));
+            sent_any = true;
           }
         }
-        if (out_of_range) atomicOr(a.err, kErrRange);
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&bars->kv_full[stage]));
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
         if (++stage == kStages) {
           stage = 0;
           ph ^= 1u;
@@ -1213,6 +1261,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       }
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
+    // After an abort the peer may leave soon: give a copy just issued to it
+    // time to land (copies take microseconds) before this CTA reaches the end.
+    if (!ok && sent_any)
+      for (int i = 0; i < 100; ++i) __nanosleep(1000);
   }
 
   __syncwarp();
@@ -1261,15 +1313,16 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters) {
   return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<false>, &cfg);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map9, const CUtensorMap& kv_map8,
-                          const CUtensorMap& q_map, const CUtensorMap& out_map, const CUtensorMap& out_map4,
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map_s, const CUtensorMap& kv_map_a,
+                          const CUtensorMap& kv_map_r, const CUtensorMap& q_map, const CUtensorMap& out_map, const CUtensorMap& out_map4,
                           int clusters, bool fp8, cudaStream_t stream) {
   cudaError_t e = set_smem_attr(fp8);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_cfg(fp8, clusters, stream, attr, true);
-  if (fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map9, kv_map8, q_map, out_map, out_map4, a);
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map9, kv_map8, q_map, out_map, out_map4, a);
+  if (fp8)
+    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map, out_map4, a);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map, out_map4, a);
 }
 
 }  // namespace mla_gb300

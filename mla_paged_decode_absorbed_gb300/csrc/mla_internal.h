@@ -11,6 +11,7 @@ constexpr int kDqk = 576;            // channels per query head / KV token (512 
 constexpr int kDv = 512;             // output channels (latent part of a KV row)
 constexpr int kRowsPerBlock = 128;   // query rows (token-major (i, h)) per work unit = MMA M
 constexpr int kGroups = 5;           // fp8 scale groups per token
+constexpr int kFp8ScorerBlocks = 3;  // fp8: latent 64-channel blocks the scorer converts (rest: accumulator)
 constexpr int kDefaultOverhead = 2;  // planner cost per work unit, in pages
 // A split unit with at most this many pieces is merged inside the attention
 // kernel by the piece that finishes last; units with more pieces are merged by
@@ -71,8 +72,8 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters);
 // (64, 32, 1) is 32 rows x 64 channels (rows past R are not written).
 // out_map4: out as a 4-D tensor (64 channels, R rows, 8 channel chunks, B)
 // whose box (64, 32, 4, 1) is 32 rows x 256 channels.
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map9, const CUtensorMap& kv_map8,
-                          const CUtensorMap& q_map, const CUtensorMap& out_map, const CUtensorMap& out_map4,
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map_s, const CUtensorMap& kv_map_a,
+                          const CUtensorMap& kv_map_r, const CUtensorMap& q_map, const CUtensorMap& out_map, const CUtensorMap& out_map4,
                           int clusters, bool fp8, cudaStream_t stream);
 
 }  // namespace mla_gb300

@@ -282,6 +282,17 @@ __device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* gsrc, u
       : "memory");
 }
 
+// Bulk copy from this CTA's shared memory into a peer CTA's (cluster
+// address), completing `bytes` transaction bytes on the peer's mbarrier
+// `remote_bar` (both addresses 16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_copy_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                               uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src_cta), "r"(bytes), "r"(remote_bar)
+               : "memory");
+}
+
 // Bulk prefetch of global memory into L2 (address and size 16-byte aligned).
 __device__ __forceinline__ void prefetch_l2(const void* gsrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
