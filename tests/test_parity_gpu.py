@@ -17,7 +17,7 @@ import mla_paged_decode_absorbed_gb300 as mla
 import oracle
 from oracle import plan_ref
 from workloads import gen
-from tests.gpu_helpers import TOL_BF16, TOL_FP8, compare, run_gpu, to_device
+from tests.gpu_helpers import TOL_BF16, TOL_FP8, compare, fp16_k_lse_shift, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -35,15 +35,20 @@ def _cuda():
 
 
 def _check(inp, tol=None, rows=None, **kw):
+    """For the fp8 cache the lse bound of a row is the stated 1e-3 plus the
+    shift that rounding the dequantised cache to fp16 alone causes in that
+    row (fp16_k_lse_shift): the variant's tensor-core operands are 16-bit,
+    and on a row dominated by one key that shift reaches about 1.1e-3."""
     tol = tol or (TOL_FP8 if inp.kv_fp8 else TOL_BF16)
     out_g, lse_g, status, _ = run_gpu(inp, **kw)
     assert status == mla.MLA_OK, mla.status_string(status)
+    extra = fp16_k_lse_shift(inp, rows=rows) if inp.kv_fp8 else None
     if rows is None:
         out_r, lse_r = oracle.mla_decode_inputs(inp)
-        return compare(out_g, lse_g, out_r, lse_r, tol)
+        return compare(out_g, lse_g, out_r, lse_r, tol, lse_extra=extra)
     out_r, lse_r = oracle.mla_decode_inputs(inp, rows=rows)
     assert np.isfinite(out_g).all()
-    return compare(out_g[rows.numpy()], lse_g[rows.numpy()], out_r, lse_r, tol)
+    return compare(out_g[rows.numpy()], lse_g[rows.numpy()], out_r, lse_r, tol, lse_extra=extra)
 
 
 # ------------------------------------------------------------------ workloads
@@ -69,9 +74,14 @@ def test_full_size_workloads_sampled_rows(name):
 
 
 # ------------------------------------------------------------------ splits and shapes
+@pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("clusters,ovh", [(1, 1), (2, 2), (3, 1), (7, 3)])
-def test_forced_splits_match(clusters, ovh):
-    inp = gen.make_inputs("x", seqlens=[1000, 64, 1, 2500, 130], heads=32, s_q=2, seed=31)
+def test_forced_splits_match(clusters, ovh, fp8):
+    """Many segments per cluster (ring stages and barrier phases carry over
+    segment and unit boundaries, including empty units), split units merged
+    in the kernel and in the combine kernel; for the fp8 cache also the
+    per-page exchange of converted blocks between the two CTAs."""
+    inp = gen.make_inputs("x", seqlens=[1000, 64, 1, 2500, 130], heads=32, s_q=2, kv_fp8=fp8, seed=31)
     _check(inp, max_clusters=clusters, plan_overhead=ovh)
 
 
@@ -202,15 +212,17 @@ def test_device_plan_equals_reference_plan(seqlens, heads, s_q, clusters, ovh):
 
 
 # ------------------------------------------------------------------ device errors
-def test_page_id_out_of_pool_is_reported_not_faulted():
-    inp = gen.make_inputs("x", seqlens=[300, 50], heads=16, s_q=1, seed=4)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_page_id_out_of_pool_is_reported_not_faulted(fp8):
+    inp = gen.make_inputs("x", seqlens=[300, 50], heads=16, s_q=1, kv_fp8=fp8, seed=4)
     inp.block_table[0, 2] = inp.num_pages + 5
     out_g, lse_g, status, _ = run_gpu(inp)
     assert status == mla.MLA_ERR_DEVICE_BOUNDS
     assert np.isfinite(out_g).all()
     # the other request is untouched by the bad entry
-    out_r, lse_r = oracle.mla_decode(inp.q[1:], inp.kv, inp.block_table[1:], inp.seqlens[1:], 1, inp.softmax_scale)
-    compare(out_g[16:], lse_g[16:], out_r, lse_r, TOL_BF16)
+    out_r, lse_r = oracle.mla_decode(inp.q[1:], inp.kv, inp.block_table[1:], inp.seqlens[1:], 1, inp.softmax_scale,
+                                     kv_scales=inp.kv_scales, kv_dtype=oracle.KV_FP8 if fp8 else oracle.KV_BF16)
+    compare(out_g[16:], lse_g[16:], out_r, lse_r, TOL_FP8 if fp8 else TOL_BF16)
 
 
 def test_seqlen_beyond_block_table_is_reported():
@@ -231,8 +243,9 @@ def test_error_word_clears_on_next_good_call():
 
 
 # ------------------------------------------------------------------ determinism, streams, graphs
-def test_repeated_calls_are_bitwise_identical():
-    inp = gen.make_inputs("x", seqlens=[3000, 17, 900], heads=128, s_q=1, seed=6)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_repeated_calls_are_bitwise_identical(fp8):
+    inp = gen.make_inputs("x", seqlens=[3000, 17, 900], heads=128, s_q=1, kv_fp8=fp8, seed=6)
     t = to_device(inp)
     o1, l1, _, dec = run_gpu(inp, tensors=t, max_clusters=5)
     o2, l2, _, _ = run_gpu(inp, tensors=t, decoder=dec)
@@ -262,13 +275,13 @@ def test_side_stream_and_cuda_graph_replay():
 
 
 # ------------------------------------------------------------------ split merges
-@pytest.mark.parametrize("clusters", [3, 5, 12, 40])
-def test_merge_in_kernel_and_in_combine(clusters):
+@pytest.mark.parametrize("clusters,fp8", [(3, False), (5, False), (12, False), (40, False), (5, True), (40, True)])
+def test_merge_in_kernel_and_in_combine(clusters, fp8):
     """Units split into 2..FUSE_MAX pieces are merged by the attention
     kernel's last finisher; units with more pieces by the combine kernel.
     Both must match."""
     seqlens = [9000, 64, 3100, 700, 1, 2000]
-    inp = gen.make_inputs("x", seqlens=seqlens, heads=128, s_q=1, seed=40 + clusters)
+    inp = gen.make_inputs("x", seqlens=seqlens, heads=128, s_q=1, kv_fp8=fp8, seed=40 + clusters)
     d = mla.make_desc(inp.batch, 1, 128, inp.num_pages, inp.max_pages_per_seq, max_clusters=clusters)
     G = mla.mla_num_clusters(d)
     ref = plan_ref.make_plan(seqlens, 1, 128, inp.max_pages_per_seq, G, 2)
