@@ -21,6 +21,7 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kCombineChunksPerCta = 4;  // 8-channel chunks of every row per combine CTA
 constexpr int kCombineThreads = 128 * kCombineChunksPerCta;
+constexpr int kCombineJobColumns = 4;     // CTA columns of the combine grid (they stride over jobs)
 
 // ------------------------------------------------------------------ planner
 // Cost of unit u (row block rb = u / B of request b = u % B): the pages the
@@ -125,28 +126,13 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
 }
 
 // ------------------------------------------------------------------ combine
-// Units with at most kFuseMax pieces are merged inside the attention kernel;
-// this kernel merges the others.  CTA (c, y): the unit whose pages start in
-// cluster c's range and continue past it (at most one per cluster), 8-channel
-// chunks [2y, 2y + 2) of every row (one row per thread, so the chunk-
-// interleaved fp16 partial slots are read with coalesced loads):
-//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
-// where out_k = stored_k * scale_k.  Two passes over the pieces (lse max,
-// then the weighted sum), so all loads of a pass are independent.
-__global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
-  // launched as a programmatic dependent of the attention kernel: wait for it
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // one CTA column per job (the planner marks unused job slots with unit -1)
-  const int4 job = reinterpret_cast<const int4*>(a.sync + 4 * a.clusters)[blockIdx.x];
-  if (job.x < 0) return;
+// One combine job, one 8-channel chunk `j` of row L of the unit's row block.
+__device__ __forceinline__ void combine_rows(const CombineArgs& a, const float2* lp, const uint4* op, int4 job,
+                                             int L, int j) {
   const int u = job.x, c = job.y, last = job.z, slot0 = job.w;
   const int b = u % a.B, rb = u / a.B;
-  const int L = threadIdx.x & (kRowsPerBlock - 1);                      // row within the block
-  const int j = blockIdx.y * kCombineChunksPerCta + (threadIdx.x >> 7);  // 8-channel chunk
   const int r = rb * kRowsPerBlock + L;
   if (r >= a.R) return;
-  const float2* lp = reinterpret_cast<const float2*>(a.lse_part);
-  const uint4* op = reinterpret_cast<const uint4*>(a.o_part);
   // pieces in batches of 8 (all loads of a batch issued together), with a
   // running max across batches
   float mx = -INFINITY, wsum = 0.f;
@@ -200,6 +186,31 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   reinterpret_cast<uint4*>(a.out + orow * kDv)[j] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   if (j == 0) a.lse[orow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
+
+// Units with at most kFuseMax pieces are merged inside the attention kernel;
+// this kernel merges the others (the planner's job list: unit, first and last
+// cluster, slot of the first piece).  CTA (x, y) takes jobs x, x + gridDim.x,
+// ... and 8-channel chunks [4y, 4y + 4) of every row, one row per thread, so
+// the chunk-interleaved fp16 partial slots are read with coalesced loads:
+//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
+// where out_k = stored_k * scale_k.  Pieces go in batches of 8 whose loads
+// are all issued together, with a running maximum across batches.
+__global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
+  // launched as a programmatic dependent of the attention kernel: wait for it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // CTA columns stride over the jobs; the planner packs them in front of the
+  // unused slots, which hold unit -1
+  const int L = threadIdx.x & (kRowsPerBlock - 1);                      // row within the block
+  const int j = blockIdx.y * kCombineChunksPerCta + (threadIdx.x >> 7);  // 8-channel chunk
+  const float2* lp = reinterpret_cast<const float2*>(a.lse_part);
+  const uint4* op = reinterpret_cast<const uint4*>(a.o_part);
+  for (int jb = blockIdx.x; jb < a.clusters; jb += gridDim.x) {
+    const int4 job = reinterpret_cast<const int4*>(a.sync + 4 * a.clusters)[jb];
+    if (job.x < 0) return;
+    combine_rows(a, lp, op, job, L, j);
+  }
+}
+
 
 // ------------------------------------------------------------------ host helpers
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -511,8 +522,11 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   // programmatic dependent of the attention kernel (it waits on the device)
   cudaLaunchConfig_t cfg = {};
   // a job unit has more than kFuseMax pieces, so it spans at least kFuseMax of
-  // the G - 1 cluster boundaries: there are at most (G - 1) / kFuseMax jobs
-  cfg.gridDim = dim3(p.G > kFuseMax ? (p.G - 1) / kFuseMax : 1, kPartChunks / kCombineChunksPerCta, 1);
+  // the G - 1 cluster boundaries: there are at most (G - 1) / kFuseMax jobs.
+  // A few CTA columns stride over them: a grid sized for the worst case cost
+  // several microseconds per step to schedule even when there is no job.
+  const int max_jobs = p.G > kFuseMax ? (p.G - 1) / kFuseMax : 1;
+  cfg.gridDim = dim3(max_jobs < kCombineJobColumns ? max_jobs : kCombineJobColumns, kPartChunks / kCombineChunksPerCta, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
