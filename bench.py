@@ -47,6 +47,7 @@ WORKLOAD_TEXT = {
     "tiny": "tiny: B=2 s_q=1 H=16 seqlens {37,130}, bf16 cache, page 64",
     "decode": "decode: B=64 s_q=1 H=128 seqlens U[1024,4096], bf16 q and latent cache, page 64, scale 1/sqrt(192)",
     "mtp": "MTP verify: B=128 s_q=2 (causal) H=128 seqlen 4096, bf16, page 64",
+    "mtp6": "MTP verify of five draft tokens: B=64 s_q=6 (causal) H=128 seqlen 4096, bf16, page 64",
     "long": "long skewed: B=16 s_q=1 H=128 lognormal seqlens (mean 3500, sigma 1) + one 65536, bf16, page 64",
     "fp8": "fp8 cache: B=256 s_q=2 (causal) H=128 seqlen 2048, e4m3 cache + fp32 scale per token per 128-ch group",
 }

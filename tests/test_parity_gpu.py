@@ -66,7 +66,7 @@ def test_reduced_workloads_every_output(name, kw):
     _check(gen.make_inputs(name, **kw))
 
 
-@pytest.mark.parametrize("name", ["decode", "mtp", "long", "fp8"])
+@pytest.mark.parametrize("name", ["decode", "mtp", "long", "fp8", "mtp6"])
 def test_full_size_workloads_sampled_rows(name):
     inp = gen.make_inputs(name)
     rows = gen.sample_rows(inp, 160)
@@ -95,6 +95,8 @@ def test_forced_splits_match(clusters, ovh, fp8):
     ([200], 128, 16, False),             # 16 row blocks, causal across blocks
     ([65, 3, 128], 16, 1, True),         # fp8 tails and a 3-key request
     ([333], 40, 5, True),                # fp8 with causal verify of 5 tokens
+    ([4096, 700, 3], 128, 6, False),     # five draft tokens, 768 rows per request, a request shorter than s_q
+    ([2000, 5, 130], 128, 6, True),      # the same with the fp8 cache
 ])
 def test_edge_shapes(seqlens, heads, s_q, fp8):
     _check(gen.make_inputs("x", seqlens=seqlens, heads=heads, s_q=s_q, kv_fp8=fp8, seed=sum(seqlens) + heads))

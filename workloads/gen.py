@@ -46,7 +46,7 @@ D_V = 512          # output channels (the latent part of each KV row)
 FP8_GROUPS = ((0, 128), (128, 256), (256, 384), (384, 512), (512, 576))
 SOFTMAX_SCALE = 1.0 / math.sqrt(192.0)
 
-WORKLOADS = ("tiny", "decode", "mtp", "long", "fp8")
+WORKLOADS = ("tiny", "decode", "mtp", "long", "fp8", "mtp6")
 
 
 @dataclasses.dataclass
@@ -66,6 +66,8 @@ def workload_spec(name: str) -> Workload:
         "mtp": (128, 2, 128, False),
         "long": (16, 1, 128, False),
         "fp8": (256, 2, 128, True),
+        # five draft tokens per request (s_q = 6, 768 query rows per request)
+        "mtp6": (64, 6, 128, False),
     }
     if name not in table:
         raise KeyError(f"unknown workload {name!r}; known: {WORKLOADS}")
@@ -114,6 +116,8 @@ def _seqlens_for(name: str, batch: int, g: torch.Generator) -> torch.Tensor:
         return s
     if name == "fp8":
         return torch.full((batch,), 2048, dtype=torch.int32)
+    if name == "mtp6":
+        return torch.full((batch,), 4096, dtype=torch.int32)
     raise KeyError(name)
 
 
