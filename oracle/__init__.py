@@ -6,7 +6,8 @@ CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library in
 two share no code: the oracle is plain fp64 C (``mla_oracle.c``) compiled with
 gcc, loaded here with ctypes.
 
-Pinned by ``tests/test_oracle_pins.py`` against: the non-absorbed MLA form,
+Pinned by ``tests/test_oracle_pins.py`` against: the non-absorbed MLA form
+(which also pins ``absorb_q`` and ``project_out``, the absorption GEMMs),
 closed forms (single key, identical keys, a hand-derived two-key example),
 softmax rows summing to one, the split/LSE-merge identity, the batch-extension
 equivalence of causal verify, a dense library softmax, and torch's bf16/e4m3
@@ -148,3 +149,35 @@ def mla_decode_inputs(inp, rows=None, return_p: bool = False):
     return mla_decode(inp.q, inp.kv, inp.block_table, inp.seqlens, inp.s_q, inp.softmax_scale,
                       kv_scales=inp.kv_scales, kv_dtype=KV_FP8 if inp.kv_fp8 else KV_BF16, rows=rows,
                       return_p=return_p)
+
+
+# ------------------------------------------------------- absorption GEMMs
+# Matrix absorption for MLA (best-practice digest §2.4.3, the
+# `--mla_use_matrix_absorption` switch; the algebra is standard MLA): the key
+# up-projection W_UK is folded into the query and the value up-projection W_UV
+# is applied to the latent output.  Plain fp64 definitions.
+
+def _f64(t) -> np.ndarray:
+    """Values of ``t`` (torch tensor of any float dtype, or array) in fp64."""
+    import torch
+    if isinstance(t, torch.Tensor):
+        return t.detach().cpu().to(torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def absorb_q(q_nope, q_rope, w_uk) -> np.ndarray:
+    """q[t, h] = [W_UK[h] @ q_nope[t, h] ; q_rope[t, h]]  (fp64 [T, H, 576]).
+
+    q_nope [T, H, 128], q_rope [T, H, 64], w_uk [H, 512, 128] (any float or
+    bf16 tensor/array; bf16 values are taken exactly)."""
+    qn, qr, w = _f64(q_nope), _f64(q_rope), _f64(w_uk)
+    lat = np.einsum("hcd,thd->thc", w, qn)
+    return np.concatenate([lat, qr], axis=-1)
+
+
+def project_out(out_latent, w_uv) -> np.ndarray:
+    """o[t, h] = W_UV[h]^T @ out_latent[t, h]  (fp64 [T, H, 128]).
+
+    out_latent [T, H, 512], w_uv [H, 512, 128]."""
+    o, w = _f64(out_latent), _f64(w_uv)
+    return np.einsum("hcd,thc->thd", w, o)

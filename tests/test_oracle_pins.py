@@ -75,9 +75,11 @@ def test_absorbed_equals_non_absorbed_mla(s_q):
     q_rope = rng.standard_normal((B, s_q, H, 64))
 
     # absorbed inputs: q_h = [W_UK_h q_nope_h ; q_rope_h], KV row = [c_t ; k_rope_t]
-    q_abs = np.concatenate([np.einsum("hcd,bihd->bihc", W_UK, q_nope), q_rope], axis=-1)
+    q_abs = oracle.absorb_q(q_nope.reshape(B * s_q, H, 128), q_rope.reshape(B * s_q, H, 64),
+                            W_UK).reshape(B, s_q, H, 576)
     kv = np.concatenate([latent, krope], axis=-1)
     out_abs, lse_abs = oracle.mla_decode(q_abs, kv, bt, seqlens, s_q, SCALE, kv_dtype=KV_F64)
+    o_abs = oracle.project_out(out_abs.reshape(B * s_q, H, 512), W_UV).reshape(B, s_q, H, 128)
     out_abs = out_abs.reshape(B, s_q, H, 512)
     lse_abs = lse_abs.reshape(B, s_q, H)
 
@@ -95,6 +97,7 @@ def test_absorbed_equals_non_absorbed_mla(s_q):
                 out_std = (p / p.sum()) @ v
                 lse_std = s.max() + math.log(p.sum())
                 np.testing.assert_allclose(W_UV[h].T @ out_abs[b, i, h], out_std, rtol=1e-10, atol=1e-12)
+                np.testing.assert_allclose(o_abs[b, i, h], out_std, rtol=1e-10, atol=1e-12)
                 assert abs(lse_abs[b, i, h] - lse_std) < 1e-10
 
 
