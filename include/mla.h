@@ -187,6 +187,41 @@ mla_status mla_decode_noalloc(const mla_desc* desc, const void* q, const void* k
                               const int32_t* block_table, const int32_t* seqlens, int32_t s_q, float softmax_scale,
                               void* out, float* lse, int check_device_error, void* stream);
 
+/*
+ * Matrix absorption around the attention step (best-practice digest §2.4.3:
+ * the --mla_use_matrix_absorption switch of the DeepSeek deployment scripts;
+ * the pages give only the switch, the algebra is standard MLA).  With
+ * per-head up-projections W_UK[h], W_UV[h] of shape [512, 128] (latent x
+ * head dim), attention over the latent cache with an absorbed query equals
+ * standard MLA attention:
+ *
+ *   mla_absorb_q:     q[t, h, 0:512]   = W_UK[h] @ q_nope[t, h]      (128 -> 512)
+ *                     q[t, h, 512:576] = q_rope[t, h]
+ *   mla_project_out:  o[t, h]          = W_UV[h]^T @ out[t, h]       (512 -> 128)
+ *
+ * t runs over the `tokens` = B * s_q token rows in mla_decode()'s order
+ * (b-major, then i), so q and out are exactly mla_decode()'s q and out.
+ * Both are per-head tcgen05 GEMMs with fp32 accumulation and bf16 results.
+ *
+ *   q_nope     device, bf16 [tokens, H, 128], contiguous, 16-byte aligned
+ *   q_rope     device, bf16 [tokens, H, 64], contiguous, 16-byte aligned
+ *   w_uk, w_uv device, bf16 [H, 512, 128], contiguous, 16-byte aligned
+ *   q          device, bf16 [tokens, H, 576], 16-byte aligned (written)
+ *   out        device, bf16 [tokens, H, 512], 16-byte aligned
+ *   o          device, bf16 [tokens, H, 128], 16-byte aligned (written)
+ *   tokens     >= 1;  num_heads 1..1024
+ *   workspace  an mla_decode() workspace whose error word records a pipeline
+ *              timeout (MLA_ERR_DEVICE_TIMEOUT through mla_get_device_error()),
+ *              or NULL; 256-byte aligned when given
+ *
+ * Host-visible problems return a negative status and launch nothing; the
+ * call is asynchronous on `stream` and allocates nothing.
+ */
+mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const void* w_uk, int32_t tokens,
+                        int32_t num_heads, void* q, void* workspace, void* stream);
+mla_status mla_project_out(const void* out, const void* w_uv, int32_t tokens, int32_t num_heads, void* o,
+                           void* workspace, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* mla_status_string(int status);
 

@@ -94,6 +94,10 @@ def _load():
             lib.mla_get_device_error.argtypes = [vp, vp]
             lib.mla_status_string.restype = ctypes.c_char_p
             lib.mla_status_string.argtypes = [ctypes.c_int]
+            lib.mla_absorb_q.restype = ctypes.c_int
+            lib.mla_absorb_q.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp]
+            lib.mla_project_out.restype = ctypes.c_int
+            lib.mla_project_out.argtypes = [vp, vp, i32, i32, vp, vp, vp]
             lib.mla_get_workspace_layout.restype = ctypes.c_int
             lib.mla_get_workspace_layout.argtypes = [dp, ctypes.c_int, ctypes.POINTER(MlaWorkspaceLayout)]
             _lib = lib
@@ -183,6 +187,29 @@ def mla_decode(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, 
     _check(_load().mla_decode(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table),
                               _ptr(seqlens), int(s_q), float(softmax_scale), _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel(), _stream(stream)), "mla_decode")
+
+
+def mla_absorb_q(q_nope, q_rope, w_uk, q, workspace=None, stream=None) -> None:
+    """q[t, h] = [W_UK[h] @ q_nope[t, h] ; q_rope[t, h]] (bf16 tensors:
+    q_nope [T, H, 128], q_rope [T, H, 64], w_uk [H, 512, 128], q [T, H, 576])."""
+    T, H = int(q_nope.shape[0]), int(q_nope.shape[1])
+    _expect(q_nope, "q_nope", torch.bfloat16, (T, H, 128))
+    _expect(q_rope, "q_rope", torch.bfloat16, (T, H, 64))
+    _expect(w_uk, "w_uk", torch.bfloat16, (H, 512, 128))
+    _expect(q, "q", torch.bfloat16, (T, H, 576))
+    _check(_load().mla_absorb_q(_ptr(q_nope), _ptr(q_rope), _ptr(w_uk), T, H, _ptr(q), _ptr(workspace),
+                                _stream(stream)), "mla_absorb_q")
+
+
+def mla_project_out(out, w_uv, o, workspace=None, stream=None) -> None:
+    """o[t, h] = W_UV[h]^T @ out[t, h] (bf16 tensors: out [T, H, 512],
+    w_uv [H, 512, 128], o [T, H, 128])."""
+    T, H = int(out.shape[0]), int(out.shape[1])
+    _expect(out, "out", torch.bfloat16, (T, H, 512))
+    _expect(w_uv, "w_uv", torch.bfloat16, (H, 512, 128))
+    _expect(o, "o", torch.bfloat16, (T, H, 128))
+    _check(_load().mla_project_out(_ptr(out), _ptr(w_uv), T, H, _ptr(o), _ptr(workspace), _stream(stream)),
+           "mla_project_out")
 
 
 def mla_get_device_error(workspace: torch.Tensor, stream=None) -> int:

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libmla_gb300.so")
-SOURCES = ["mla_decode_kernel.cu", "mla_abi.cu", "mla_noalloc.cu"]
+SOURCES = ["mla_decode_kernel.cu", "mla_abi.cu", "mla_noalloc.cu", "mla_absorb.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

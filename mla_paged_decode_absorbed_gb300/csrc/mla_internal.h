@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <cstdint>
 
 namespace mla_gb300 {
@@ -59,13 +60,20 @@ struct CombineArgs {
   int B, R, U, clusters, overhead;
 };
 
+// mla_abi.cu: the driver's tensor-map encoder (null if it cannot be found).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 // mla_decode_kernel.cu
 int decode_smem_bytes(bool fp8);
 cudaError_t decode_max_active_clusters(bool fp8, int* clusters);
-// kv_map9 / kv_map8: the cache as a 4-D tensor (64 channels, 64 tokens, 9
-// channel chunks, pages) with a chunk stride of 128 bytes; one box brings
-// chunks 0..8 (scorer) or 0..7 (accumulator) of a page, laid out in shared
-// memory as consecutive 64-token x 64-channel swizzled blocks.
+// kv_map_s / kv_map_a: the page maps of the scorer and the accumulator.  bf16
+// cache: the cache as a 4-D tensor (64 channels, 64 tokens, 9 channel chunks,
+// pages) with a chunk stride of 128 bytes; one box brings chunks 0..8 (scorer)
+// or 0..7 (accumulator) of a page as consecutive 64-token x 64-channel
+// swizzled blocks.  fp8 cache: the e4m3 bytes as a 4-D tensor (64 bytes, 64
+// tokens, 9 chunks, pages), 64-byte swizzled; boxes of kFp8ScorerBlocks
+// (scorer) or 8 - kFp8ScorerBlocks (accumulator) chunks, and kv_map_r one
+// chunk (the scorer's RoPE chunk).  kv_map_r is unused for the bf16 cache.
 // q_map: q as a 4-D tensor (64 channels, 9 channel chunks, R rows, B) whose
 // box (64, 9, 64, 1) is half a row block (rows past R read as zeros).
 // out_map: out as a 3-D tensor (512 channels, R rows, B) whose box

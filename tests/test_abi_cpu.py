@@ -183,3 +183,20 @@ def test_reference_plan_on_named_workloads():
         else:
             plan = plan_ref.make_plan(inp.seqlens.tolist(), 1, 16, inp.max_pages_per_seq, 76, 2)
         _check_plan(plan)
+
+
+def test_absorption_entry_points_reject_bad_arguments_without_a_gpu(lib):
+    """Host validation of mla_absorb_q / mla_project_out returns
+    MLA_ERR_INVALID_ARG and launches nothing (no device memory is touched:
+    the pointers below are never dereferenced)."""
+    A = 1 << 20  # a 16-byte aligned fake address
+    bad = mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_absorb_q(A, A, A, 0, 4, A, None, None) == bad          # no tokens
+    assert lib.mla_absorb_q(A, A, A, 3, 0, A, None, None) == bad          # no heads
+    assert lib.mla_absorb_q(A, A, A, 3, 2000, A, None, None) == bad       # too many heads
+    assert lib.mla_absorb_q(None, A, A, 3, 4, A, None, None) == bad       # NULL input
+    assert lib.mla_absorb_q(A + 8, A, A, 3, 4, A, None, None) == bad      # misaligned q_nope
+    assert lib.mla_absorb_q(A, A, A, 3, 4, A, A + 16, None) == bad        # workspace not 256-aligned
+    assert lib.mla_project_out(A, A, 0, 4, A, None, None) == bad
+    assert lib.mla_project_out(A, None, 3, 4, A, None, None) == bad
+    assert lib.mla_project_out(A, A, 3, 4, A + 2, None, None) == bad
