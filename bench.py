@@ -235,6 +235,46 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def absorption_gemms(inp, flush, hbm_gbs, tflops_peak, iters: int = 10):
+    """Times the absorption GEMMs (mla_absorb_q, mla_project_out) on this
+    workload's token rows (B*s_q) and heads, with random bf16 weights of the
+    MLA shape (H x 512 x 128), L2 flushed before each launch.  Each is HBM-bound
+    on its weights at few tokens and tensor-bound at many; reported against
+    the bound that applies."""
+    import mla_paged_decode_absorbed_gb300 as mla
+    T, H = inp.batch * inp.s_q, inp.heads
+    g = torch.Generator(device="cuda").manual_seed(4242)
+    rn = lambda *shape: (torch.randn(shape, device="cuda", generator=g) / 8).to(torch.bfloat16)
+    q_nope, q_rope, w_uk, w_uv, outl = rn(T, H, 128), rn(T, H, 64), rn(H, 512, 128), rn(H, 512, 128), rn(T, H, 512)
+    q = torch.empty((T, H, 576), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty((T, H, 128), dtype=torch.bfloat16, device="cuda")
+    res = {}
+    for name, fn, nbytes in (
+            ("absorb_q", lambda: mla.mla_absorb_q(q_nope, q_rope, w_uk, q), H * 512 * 128 * 2 + T * H * (192 + 576) * 2),
+            ("project_out", lambda: mla.mla_project_out(outl, w_uv, o), H * 512 * 128 * 2 + T * H * (512 + 128) * 2)):
+        flops = 2.0 * T * H * 512 * 128
+        for _ in range(3):
+            fn()
+        times = []
+        for it in range(iters):
+            flush.fill_(it & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = sorted(times)[len(times) // 2]
+        hbm = nbytes / (hbm_gbs * 1e9) >= flops / (tflops_peak * 1e12)
+        ach = (nbytes / (ms * 1e-3) / 1e9) if hbm else (flops / (ms * 1e-3) / 1e12)
+        peak = hbm_gbs if hbm else tflops_peak
+        res[name] = {"us": ms * 1e3, "bound": "hbm" if hbm else "tensor", "achieved": ach,
+                     "unit": "GB/s" if hbm else "TFLOP/s", "peak": peak, "frac": ach / peak,
+                     "algorithmic_bytes": nbytes, "flops": flops}
+    res["shape"] = f"tokens={T} heads={H}, weights [H,512,128] bf16, L2 flushed before each launch"
+    return res
+
+
 def cpu_baseline(inp, seconds: float = 12.0):
     """Time the oracle on a bounded sample of the workload (rank 0, N=1):
     about `seconds` of host work; a sample smaller than that is repeated."""
@@ -423,6 +463,7 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
+    line["absorption_gemms"] = absorption_gemms(inp, flush, hbm_gbs, tflops_peak)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
     print(json.dumps(line), flush=True)
