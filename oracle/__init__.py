@@ -29,7 +29,7 @@ _LIB = os.path.join(_HERE, "_liboracle_mla.so")
 _lock = threading.Lock()
 _lib = None
 
-KV_BF16, KV_FP8, KV_F64 = 0, 1, 2
+KV_BF16, KV_FP8, KV_F64, KV_FP8B = 0, 1, 2, 3  # KV_FP8B: fp8 variant B, [P, 64, 656] token records
 
 
 def build(force: bool = False) -> str:
@@ -114,6 +114,8 @@ def mla_decode(q, kv, block_table, seqlens, s_q: int, softmax_scale: float, *, k
     else:
         qa = _np(q, np.uint16)
         kva = _np(kv, np.uint16 if kv_dtype == KV_BF16 else np.uint8)
+        if kv_dtype == KV_FP8B and (kva.ndim != 3 or kva.shape[2] != 656):
+            raise ValueError("fp8 variant B cache must be uint8 [P, 64, 656]")
     sca = _np(kv_scales, np.float32) if kv_scales is not None else None
     bta = _np(block_table, np.int32)
     sla = _np(seqlens, np.int32)
@@ -146,9 +148,9 @@ def mla_decode(q, kv, block_table, seqlens, s_q: int, softmax_scale: float, *, k
 
 def mla_decode_inputs(inp, rows=None, return_p: bool = False):
     """Oracle on a ``workloads.gen.Inputs`` bundle."""
+    dt = (KV_FP8B if getattr(inp, "rope_bf16", False) else KV_FP8) if inp.kv_fp8 else KV_BF16
     return mla_decode(inp.q, inp.kv, inp.block_table, inp.seqlens, inp.s_q, inp.softmax_scale,
-                      kv_scales=inp.kv_scales, kv_dtype=KV_FP8 if inp.kv_fp8 else KV_BF16, rows=rows,
-                      return_p=return_p)
+                      kv_scales=inp.kv_scales, kv_dtype=dt, rows=rows, return_p=return_p)
 
 
 # ------------------------------------------------------- absorption GEMMs

@@ -23,7 +23,9 @@
  *
  * n <= 0 gives out = 0 and lse = -inf.  For the fp8 cache, k_t[c] is the e4m3
  * value times the fp32 scale of its token and channel group (groups of 128
- * channels, the last one 64 wide).
+ * channels, the last one 64 wide).  For fp8 variant B each token is one
+ * 656-byte record: latent channel c < 512 is its e4m3 code times the record's
+ * fp32 scale c/128, and the RoPE channels are bf16 values stored in the record.
  *
  * Every value is computed in double from the exact input values, as plain
  * loops, parallel over query rows with OpenMP.
@@ -41,7 +43,9 @@
 #define ORC_DV 512
 #define ORC_NGROUP 5
 
-enum { ORC_KV_BF16 = 0, ORC_KV_FP8 = 1, ORC_KV_F64 = 2 };
+enum { ORC_KV_BF16 = 0, ORC_KV_FP8 = 1, ORC_KV_F64 = 2, ORC_KV_FP8B = 3 };
+/* fp8 variant B token record: e4m3 latent [0,512), 4 fp32 scales [512,528), RoPE bf16 [528,656) */
+enum { ORC_FP8B_RECORD = 656 };
 enum { ORC_OK = 0, ORC_BAD_ARG = -1, ORC_BAD_PAGE = -2, ORC_NOMEM = -3 };
 
 /* bf16 -> double: a bf16 is the upper 16 bits of an IEEE binary32. */
@@ -102,6 +106,16 @@ static int fetch_key(const orc_args* a, int b, int t, double* k) {
     const uint8_t* kv = (const uint8_t*)a->kv;
     const float* sc = a->scales + ((int64_t)page * ORC_PAGE + slot) * ORC_NGROUP;
     for (int c = 0; c < ORC_DQK; ++c) k[c] = oracle_e4m3_to_f64(kv[base + c]) * (double)sc[fp8_group(c)];
+  } else if (a->kv_dtype == ORC_KV_FP8B) {
+    const uint8_t* rec = (const uint8_t*)a->kv + ((int64_t)page * ORC_PAGE + slot) * ORC_FP8B_RECORD;
+    float sc[4];
+    memcpy(sc, rec + 512, sizeof(sc));
+    for (int c = 0; c < 512; ++c) k[c] = oracle_e4m3_to_f64(rec[c]) * (double)sc[c / 128];
+    for (int c = 512; c < ORC_DQK; ++c) {
+      uint16_t v;
+      memcpy(&v, rec + 528 + 2 * (c - 512), sizeof(v));
+      k[c] = oracle_bf16_to_f64(v);
+    }
   } else {
     const double* kv = (const double*)a->kv;
     for (int c = 0; c < ORC_DQK; ++c) k[c] = kv[base + c];
@@ -164,7 +178,7 @@ int oracle_mla_decode(const void* q, const void* kv, const float* kv_scales, int
   if (!q || !kv || !block_table || !seqlens || !out || !lse) return ORC_BAD_ARG;
   if (B < 1 || s_q < 1 || H < 1 || num_pages < 1 || max_pages < 1) return ORC_BAD_ARG;
   if (kv_dtype == ORC_KV_FP8 && !kv_scales) return ORC_BAD_ARG;
-  if (kv_dtype < 0 || kv_dtype > 2) return ORC_BAD_ARG;
+  if (kv_dtype < 0 || kv_dtype > 3) return ORC_BAD_ARG;
   orc_args a = {q, kv, kv_scales, kv_dtype, block_table, seqlens, B, s_q, H, num_pages, max_pages,
                 softmax_scale};
   const int64_t total = (int64_t)B * s_q * H;

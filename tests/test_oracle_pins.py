@@ -297,3 +297,45 @@ def test_fp8_helper_dequantisation_matches_the_oracle_code_path():
     assert np.array_equal(o_f, o_c) and np.array_equal(l_f, l_c)
     shift = fp16_k_lse_shift(inp)
     assert shift.shape == l_c.shape and (shift >= 0).all() and shift.max() < 5e-3
+
+
+def test_fp8_variant_b_records_decode_like_torch():
+    """The oracle's fp8 variant B path (656-byte token records) equals its
+    fp64 path on the same cache decoded independently with torch: e4m3 codes
+    with float8_e4m3fn, the scales as float32, the RoPE as bfloat16."""
+    inp = gen.make_inputs("x", seqlens=[70, 5, 1], heads=8, s_q=2, kv_fp8=True, rope_bf16=True, seed=9)
+    rec = inp.kv
+    assert rec.shape[-1] == 656 and inp.kv_scales is None
+    lat = rec[:, :, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    sc = rec[:, :, 512:528].contiguous().view(torch.float32).to(torch.float64)
+    rope = rec[:, :, 528:].contiguous().view(torch.bfloat16).to(torch.float64)
+    dense = torch.cat([lat * sc.repeat_interleave(128, dim=-1), rope], dim=-1)
+    o_f, l_f = oracle.mla_decode(inp.q.to(torch.float64), dense, inp.block_table, inp.seqlens, inp.s_q,
+                                 inp.softmax_scale, kv_dtype=KV_F64)
+    o_b, l_b = oracle.mla_decode_inputs(inp)
+    assert np.array_equal(o_f, o_b) and np.array_equal(l_f, l_b)
+    # a single key returns its own latent row (the dequantised codes)
+    one = gen.make_inputs("x", seqlens=[1], heads=2, s_q=1, kv_fp8=True, rope_bf16=True, seed=2)
+    o1, _ = oracle.mla_decode_inputs(one)
+    r0 = one.kv[int(one.block_table[0, 0]), 0]
+    want = r0[:512].contiguous().view(torch.float8_e4m3fn).to(torch.float64) * \
+        r0[512:528].contiguous().view(torch.float32).to(torch.float64).repeat_interleave(128)
+    assert np.array_equal(o1[0], want.numpy()) and np.array_equal(o1[1], want.numpy())
+
+
+def test_fp8_q_quantisation_breaks_the_lse_bound():
+    """Why there is no fp8 (kind::f8f6f4) QK path: even with the dequantised
+    cache exact, rounding q to e4m3 (per-row scale amax/448) moves lse far past
+    the 1e-3 bound; tensor-core block scales are powers of two, so the cache's
+    fp32 scales could not be applied exactly either."""
+    inp = gen.make_inputs("x", seqlens=[2048, 700], heads=64, s_q=1, kv_fp8=True, seed=3)
+    k8 = inp.kv.view(torch.float8_e4m3fn).to(torch.float64)
+    grp = torch.tensor([0] * 128 + [1] * 128 + [2] * 128 + [3] * 128 + [4] * 64)
+    exact = k8 * inp.kv_scales.to(torch.float64)[:, :, grp]
+    q = inp.q.to(torch.float64)
+    qs = q.abs().amax(dim=-1, keepdim=True).clamp_min(1e-30) / 448.0
+    q8 = (q / qs).to(torch.float8_e4m3fn).to(torch.float64) * qs
+    _, l_ex = oracle.mla_decode(q, exact, inp.block_table, inp.seqlens, 1, inp.softmax_scale, kv_dtype=KV_F64)
+    _, l_q8 = oracle.mla_decode(q8, exact, inp.block_table, inp.seqlens, 1, inp.softmax_scale, kv_dtype=KV_F64)
+    err = np.abs(np.asarray(l_q8) - np.asarray(l_ex))
+    assert err.max() > 1e-2 and np.median(err) > 1e-3

@@ -14,6 +14,9 @@ Workloads (one per named configuration):
                 sigma 1.0) clipped to [64, 32768], request 0 set to 65536
 * ``fp8``       B=256, s_q=2, H=128, every seqlen 2048, KV stored as e4m3 with
                 one fp32 scale per token per channel group
+* ``mtp6``      B=64,  s_q=6, H=128, every seqlen 4096 (five draft tokens)
+* ``fp8b``      as ``fp8``, with the cache in fp8 variant B: a 656-byte record
+                per token (e4m3 latent, 4 fp32 scales, RoPE kept bf16)
 
 Recipe (fixed, documented so a reader can regenerate any case):
 
@@ -31,6 +34,10 @@ Recipe (fixed, documented so a reader can regenerate any case):
   [512,576); scale = amax(|group|)/448 (1.0 when the group is all zero); the
   code is the e4m3 (OCP E4M3FN) value of x/scale clamped to [-448, 448],
   encoded with torch's float8_e4m3fn conversion.
+* fp8 variant B: the four latent groups are quantised the same way; the token
+  record is bytes [0,512) e4m3 latent codes, [512,528) the four fp32 scales,
+  [528,656) the 64 RoPE channels as bf16 (the fp32 draw rounded to bf16).
+  Poisoned slots hold code 0x7F, NaN scales and NaN RoPE.
 """
 from __future__ import annotations
 
@@ -44,9 +51,10 @@ PAGE = 64          # tokens per KV page
 D_QK = 576         # 512 latent + 64 RoPE channels per query head / KV token
 D_V = 512          # output channels (the latent part of each KV row)
 FP8_GROUPS = ((0, 128), (128, 256), (256, 384), (384, 512), (512, 576))
+FP8B_RECORD = 656  # fp8 variant B bytes per token: 512 e4m3 + 4 fp32 scales + 64 bf16 RoPE
 SOFTMAX_SCALE = 1.0 / math.sqrt(192.0)
 
-WORKLOADS = ("tiny", "decode", "mtp", "long", "fp8", "mtp6")
+WORKLOADS = ("tiny", "decode", "mtp", "long", "fp8", "mtp6", "fp8b")
 
 
 @dataclasses.dataclass
@@ -68,6 +76,8 @@ def workload_spec(name: str) -> Workload:
         "fp8": (256, 2, 128, True),
         # five draft tokens per request (s_q = 6, 768 query rows per request)
         "mtp6": (64, 6, 128, False),
+        # fp8 variant B: latent e4m3 with 4 group scales, RoPE kept bf16 (656 B/token)
+        "fp8b": (256, 2, 128, True),
     }
     if name not in table:
         raise KeyError(f"unknown workload {name!r}; known: {WORKLOADS}")
@@ -84,12 +94,14 @@ class Inputs:
     s_q: int
     heads: int
     q: torch.Tensor                 # bf16 [B, s_q, H, 576]
-    kv: torch.Tensor                # bf16 [P, 64, 576] or uint8 e4m3 codes [P, 64, 576]
-    kv_scales: Optional[torch.Tensor]  # fp32 [P, 64, 5] for the fp8 cache, else None
+    kv: torch.Tensor                # bf16 [P, 64, 576], uint8 e4m3 codes [P, 64, 576], or (fp8 variant B)
+                                    # uint8 [P, 64, 656] token records
+    kv_scales: Optional[torch.Tensor]  # fp32 [P, 64, 5] for the fp8 cache (variant A), else None
     block_table: torch.Tensor       # int32 [B, max_pages_per_seq], -1 = unused
     seqlens: torch.Tensor           # int32 [B]
     softmax_scale: float
     kv_fp8: bool
+    rope_bf16: bool = False         # fp8 variant B: the token record keeps RoPE in bf16
 
     @property
     def num_pages(self) -> int:
@@ -118,13 +130,15 @@ def _seqlens_for(name: str, batch: int, g: torch.Generator) -> torch.Tensor:
         return torch.full((batch,), 2048, dtype=torch.int32)
     if name == "mtp6":
         return torch.full((batch,), 4096, dtype=torch.int32)
+    if name == "fp8b":
+        return torch.full((batch,), 2048, dtype=torch.int32)
     raise KeyError(name)
 
 
 def make_inputs(name: str, *, poison: bool = True, seqlens: Optional[Sequence[int]] = None,
                 batch: Optional[int] = None, heads: Optional[int] = None, s_q: Optional[int] = None,
                 kv_fp8: Optional[bool] = None, seed: Optional[int] = None,
-                spare_frac: float = 0.05) -> Inputs:
+                spare_frac: float = 0.05, rope_bf16: Optional[bool] = None) -> Inputs:
     """Draw the inputs of workload ``name``.
 
     The keyword overrides build smaller or edge-case variants with the same
@@ -138,6 +152,9 @@ def make_inputs(name: str, *, poison: bool = True, seqlens: Optional[Sequence[in
     H = heads if heads is not None else spec.heads
     sq = s_q if s_q is not None else spec.s_q
     fp8 = kv_fp8 if kv_fp8 is not None else spec.kv_fp8
+    rb16 = rope_bf16 if rope_bf16 is not None else name == "fp8b"
+    if rb16 and not fp8:
+        raise ValueError("rope_bf16 is a layout of the fp8 cache")
     if seqlens is not None:
         sl = torch.tensor(list(seqlens), dtype=torch.int32)
         B = int(sl.numel())
@@ -173,7 +190,27 @@ def make_inputs(name: str, *, poison: bool = True, seqlens: Optional[Sequence[in
             unowned[int(bt[b, n - 1]), s % PAGE:] = True
 
     scales = None
-    if fp8:
+    if fp8 and rb16:
+        # variant B token record: e4m3 latent [0,512), 4 fp32 scales [512,528)
+        # (groups of 128 latent channels), RoPE bf16 [528,656)
+        rec = torch.empty((num_pages, PAGE, FP8B_RECORD), dtype=torch.uint8)
+        sc4 = torch.empty((num_pages, PAGE, 4), dtype=torch.float32)
+        for gi, (c0, c1) in enumerate(FP8_GROUPS[:4]):
+            grp = kv32[:, :, c0:c1]
+            amax = grp.abs().amax(dim=-1)
+            sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+            sc4[:, :, gi] = sc
+            x = (grp / sc.unsqueeze(-1)).clamp(-448.0, 448.0)
+            rec[:, :, c0:c1] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        rope = kv32[:, :, D_V:D_QK].to(torch.bfloat16)
+        if poison:
+            rec[unowned, :D_V] = 0x7F
+            sc4[unowned] = float("nan")
+            rope[unowned] = float("nan")
+        rec[:, :, D_V:D_V + 16] = sc4.contiguous().view(torch.uint8).view(num_pages, PAGE, 16)
+        rec[:, :, D_V + 16:] = rope.contiguous().view(torch.uint8).view(num_pages, PAGE, 128)
+        kv = rec
+    elif fp8:
         scales = torch.empty((num_pages, PAGE, len(FP8_GROUPS)), dtype=torch.float32)
         codes = torch.empty((num_pages, PAGE, D_QK), dtype=torch.uint8)
         for gi, (c0, c1) in enumerate(FP8_GROUPS):
@@ -193,7 +230,7 @@ def make_inputs(name: str, *, poison: bool = True, seqlens: Optional[Sequence[in
             kv[unowned] = float("nan")
 
     return Inputs(name=name, batch=B, s_q=sq, heads=H, q=q, kv=kv, kv_scales=scales,
-                  block_table=bt, seqlens=sl, softmax_scale=SOFTMAX_SCALE, kv_fp8=fp8)
+                  block_table=bt, seqlens=sl, softmax_scale=SOFTMAX_SCALE, kv_fp8=fp8, rope_bf16=rb16)
 
 
 def sample_rows(inp: Inputs, n: int, seed: int = 7) -> torch.Tensor:
