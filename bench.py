@@ -48,6 +48,7 @@ WORKLOAD_TEXT = {
     "decode": "decode: B=64 s_q=1 H=128 seqlens U[1024,4096], bf16 q and latent cache, page 64, scale 1/sqrt(192)",
     "mtp": "MTP verify: B=128 s_q=2 (causal) H=128 seqlen 4096, bf16, page 64",
     "mtp6": "MTP verify of five draft tokens: B=64 s_q=6 (causal) H=128 seqlen 4096, bf16, page 64",
+    "fp8b": "fp8 cache variant B: B=256 s_q=2 (causal) H=128 seqlen 2048, 656-byte token records (e4m3 latent, 4 fp32 scales, bf16 RoPE)",
     "long": "long skewed: B=16 s_q=1 H=128 lognormal seqlens (mean 3500, sigma 1) + one 65536, bf16, page 64",
     "fp8": "fp8 cache: B=256 s_q=2 (causal) H=128 seqlen 2048, e4m3 cache + fp32 scale per token per 128-ch group",
 }
@@ -96,7 +97,7 @@ def work_of(inp):
     cache bytes of the tokens the longest row sees."""
     flops = 0
     kv_bytes = 0
-    per_tok = 596 if inp.kv_fp8 else 1152
+    per_tok = (656 if inp.rope_bf16 else 596) if inp.kv_fp8 else 1152
     for s in inp.seqlens.tolist():
         for i in range(inp.s_q):
             n = max(0, s - inp.s_q + i + 1)
@@ -326,6 +327,7 @@ def main():
     bt = inp.block_table.to(dev)
     sl = inp.seqlens.to(dev)
     dec = mla.MlaDecoder(inp.batch, inp.s_q, inp.heads, inp.num_pages, inp.max_pages_per_seq, kv_fp8=inp.kv_fp8,
+                         rope_bf16=inp.rope_bf16,
                          device=dev)
     d = dec.desc
     ws = dec.workspace
@@ -449,7 +451,7 @@ def main():
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if not inp.kv_fp8 else "bf16 (e4m3 cache)",
+        "vs_baseline": None, "dtype": "bf16" if not inp.kv_fp8 else ("fp16 (e4m3 latent + bf16 RoPE cache)" if inp.rope_bf16 else "fp16 (e4m3 cache)"),
         "data": "synthetic (seeded, workloads/gen.py)",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "flushed between steps (512 MiB buffer write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",

@@ -57,9 +57,13 @@ typedef enum {
 
 typedef enum {
   MLA_KV_BF16 = 0,     /* kv_pages: bf16 [num_pages, 64, 576]; MMAs in bf16 */
-  MLA_KV_FP8_E4M3 = 1  /* kv_pages: e4m3 bytes [num_pages, 64, 576] + kv_scales fp32 [num_pages, 64, 5];
+  MLA_KV_FP8_E4M3 = 1, /* kv_pages: e4m3 bytes [num_pages, 64, 576] + kv_scales fp32 [num_pages, 64, 5];
                           dequantised to fp16 in the load path and MMAs in fp16 (q is converted to
                           fp16 per row with a power-of-two scale, so it cannot overflow) */
+  MLA_KV_FP8_E4M3_ROPE_BF16 = 2  /* fp8 variant B: kv_pages is [num_pages, 64, 656] bytes, one record per
+                          token: e4m3 latent codes [0,512), four fp32 scales [512,528) (latent
+                          channel groups of 128), the 64 RoPE channels as bf16 [528,656); kv_scales
+                          must be NULL.  Computed as MLA_KV_FP8_E4M3 (fp16 MMAs) */
 } mla_kv_dtype;
 
 /* Problem description.  All fields are plain sizes; unset optional fields are 0. */
@@ -97,9 +101,11 @@ int mla_num_clusters(const mla_desc* desc);
  * mla_combine(), in order on `stream`.
  *
  *   q            device, bf16 [B, s_q, H, 576], contiguous, 16-byte aligned
- *   kv_pages     device, [num_pages, 64, 576] bf16 or e4m3 bytes, contiguous, 16-byte aligned
+ *   kv_pages     device, [num_pages, 64, 576] bf16 or e4m3 bytes, or [num_pages, 64, 656] fp8
+ *                variant B records; contiguous, 16-byte aligned
  *   kv_scales    device, fp32 [num_pages, 64, 5] for MLA_KV_FP8_E4M3 (one scale per token per
- *                channel group [0,128) [128,256) [256,384) [384,512) [512,576)); NULL for bf16
+ *                channel group [0,128) [128,256) [256,384) [384,512) [512,576)); NULL for bf16 and
+ *                for fp8 variant B
  *   block_table  device, int32 [B, max_pages_per_seq]; entries at or past
  *                ceil(seqlen/64) are never read
  *   seqlens      device, int32 [B]; keys already in the cache for each request,

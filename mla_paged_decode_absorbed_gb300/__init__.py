@@ -34,6 +34,8 @@ MLA_ERR_DEVICE_RANGE = -8
 
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
+MLA_KV_FP8_E4M3_ROPE_BF16 = 2  # fp8 variant B: [P, 64, 656] token records
+FP8B_RECORD = 656
 
 PAGE, D_QK, D_V = 64, 576, 512
 
@@ -114,12 +116,16 @@ def status_string(status: int) -> str:
 
 
 def make_desc(batch: int, s_q: int, num_heads: int, num_pages: int, max_pages_per_seq: int,
-              kv_fp8: bool = False, max_clusters: int = 0, plan_overhead: int = 0) -> MlaDesc:
+              kv_fp8: bool = False, max_clusters: int = 0, plan_overhead: int = 0,
+              rope_bf16: bool = False) -> MlaDesc:
+    """rope_bf16 (with kv_fp8): fp8 variant B, 656-byte token records."""
     d = MlaDesc()
     d.batch, d.s_q, d.num_heads = batch, s_q, num_heads
     d.num_pages, d.max_pages_per_seq = num_pages, max_pages_per_seq
     d.page_size, d.d_qk, d.d_v = PAGE, D_QK, D_V
-    d.kv_dtype = MLA_KV_FP8_E4M3 if kv_fp8 else MLA_KV_BF16
+    if rope_bf16 and not kv_fp8:
+        raise ValueError("rope_bf16 is a layout of the fp8 cache")
+    d.kv_dtype = (MLA_KV_FP8_E4M3_ROPE_BF16 if rope_bf16 else MLA_KV_FP8_E4M3) if kv_fp8 else MLA_KV_BF16
     d.max_clusters, d.plan_overhead = max_clusters, plan_overhead
     return d
 
@@ -231,9 +237,10 @@ class MlaDecoder:
     """Descriptor + workspace for repeated decode calls on one configuration."""
 
     def __init__(self, batch: int, s_q: int, num_heads: int, num_pages: int, max_pages_per_seq: int,
-                 kv_fp8: bool = False, max_clusters: int = 0, plan_overhead: int = 0, device=None):
+                 kv_fp8: bool = False, max_clusters: int = 0, plan_overhead: int = 0, device=None,
+                 rope_bf16: bool = False):
         self.desc = make_desc(batch, s_q, num_heads, num_pages, max_pages_per_seq, kv_fp8, max_clusters,
-                              plan_overhead)
+                              plan_overhead, rope_bf16)
         self.device = torch.device(device or "cuda")
         with torch.cuda.device(self.device):
             self.workspace = alloc_workspace(self.desc, self.device)
@@ -246,7 +253,11 @@ class MlaDecoder:
         d = self.desc
         B, sq, H = d.batch, d.s_q, d.num_heads
         _expect(q, "q", torch.bfloat16, (B, sq, H, D_QK))
-        if d.kv_dtype == MLA_KV_FP8_E4M3:
+        if d.kv_dtype == MLA_KV_FP8_E4M3_ROPE_BF16:
+            _expect(kv, "kv", torch.uint8, (d.num_pages, PAGE, FP8B_RECORD))
+            if kv_scales is not None:
+                raise ValueError("fp8 variant B keeps its scales inside the token records")
+        elif d.kv_dtype == MLA_KV_FP8_E4M3:
             if kv.dtype == torch.float8_e4m3fn:
                 kv = kv.view(torch.uint8)
             _expect(kv, "kv", torch.uint8, (d.num_pages, PAGE, D_QK))

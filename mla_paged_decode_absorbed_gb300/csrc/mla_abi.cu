@@ -233,13 +233,15 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Dims {
   int B, s_q, H, R, n_rb, U, P, maxp, ovh;
-  bool fp8;
+  bool fp8;        // an fp8 cache (variant A or B)
+  bool rope_bf16;  // fp8 variant B: 656-byte token records with the RoPE in bf16
 };
 
 mla_status check_desc(const mla_desc* d, Dims* out) {
   if (!d) return MLA_ERR_INVALID_ARG;
   if (d->page_size != kPage || d->d_qk != kDqk || d->d_v != kDv) return MLA_ERR_UNSUPPORTED;
-  if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+  if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_FP8_E4M3 && d->kv_dtype != MLA_KV_FP8_E4M3_ROPE_BF16)
+    return MLA_ERR_UNSUPPORTED;
   if (d->batch < 1 || d->s_q < 1 || d->s_q > 16 || d->num_heads < 1 || d->num_heads > 1024) return MLA_ERR_INVALID_ARG;
   if (d->num_pages < 1 || d->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
   if (d->max_clusters < 0 || d->plan_overhead < 0) return MLA_ERR_INVALID_ARG;
@@ -254,7 +256,8 @@ mla_status check_desc(const mla_desc* d, Dims* out) {
   x.P = d->num_pages;
   x.maxp = d->max_pages_per_seq;
   x.ovh = d->plan_overhead > 0 ? d->plan_overhead : kDefaultOverhead;
-  x.fp8 = d->kv_dtype == MLA_KV_FP8_E4M3;
+  x.fp8 = d->kv_dtype == MLA_KV_FP8_E4M3 || d->kv_dtype == MLA_KV_FP8_E4M3_ROPE_BF16;
+  x.rope_bf16 = d->kv_dtype == MLA_KV_FP8_E4M3_ROPE_BF16;
   const int64_t U = static_cast<int64_t>(x.B) * x.n_rb;
   // the plan's int32 cost prefix and page*64 token indices must not overflow
   if (U * (static_cast<int64_t>(x.maxp) + x.ovh) >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
@@ -339,20 +342,25 @@ mla_status make_kv_map4(const void* kv, int num_pages, int chunks, CUtensorMap* 
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
-// fp8 cache [P, 64, 576] e4m3 as a 4-D byte tensor (64 bytes, 64 tokens, 9
-// chunks of 64 channels, pages): box (64, 64, `chunks`, 1) brings `chunks`
-// consecutive 64-channel chunks of a page as 64-token x 64-byte slots,
-// 64-byte swizzled (so that both the dequant reads and its swizzled 16-byte
-// fp16 writes are free of bank conflicts).
-mla_status make_kv_map_fp8(const void* kv, int num_pages, int chunks, CUtensorMap* map) {
+// fp8 cache as a 4-D byte tensor (64 bytes, 64 tokens, `nchunks` chunks of
+// 64 channels, pages) starting at `base`, with `token_bytes` per token:
+// variant A [P, 64, 576] e4m3 (9 chunks); variant B [P, 64, 656] records
+// (8 latent chunks at the record start; the RoPE, 2 chunks of bf16 at byte
+// 528, as its own map).  Box (64, 64, `chunks`, 1) brings `chunks`
+// consecutive chunks of a page as 64-token x 64-byte slots, 64-byte swizzled
+// (so that both the dequant reads and its swizzled 16-byte fp16 writes are
+// free of bank conflicts).
+mla_status make_kv_map_fp8(const void* base, int num_pages, int token_bytes, int nchunks, int chunks,
+                           CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return MLA_ERR_CUDA;
-  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(kPage), 9, static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[3] = {kDqk, 64, static_cast<cuuint64_t>(kDqk) * kPage};
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(nchunks),
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(token_bytes), 64, static_cast<cuuint64_t>(token_bytes) * kPage};
   cuuint32_t box[4] = {64, 64, static_cast<cuuint32_t>(chunks), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   std::memset(map, 0, sizeof(*map));
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv), dims, strides, box, es,
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
@@ -435,7 +443,9 @@ mla_status check_tensors(const Dims& x, const void* q, const void* kv, const flo
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(bt, 4) ||
       !aligned(seqlens, 4))
     return MLA_ERR_INVALID_ARG;
-  if (x.fp8) {
+  if (x.rope_bf16) {
+    if (kv_scales) return MLA_ERR_INVALID_ARG;  // the scales are inside the token records
+  } else if (x.fp8) {
     if (!kv_scales || !aligned(kv_scales, 16)) return MLA_ERR_INVALID_ARG;
   } else if (kv_scales) {
     return MLA_ERR_INVALID_ARG;
@@ -465,9 +475,16 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   {
     mla_status st;
     if (p.x.fp8) {
-      st = make_kv_map_fp8(kv, p.x.P, kFp8ScorerBlocks, &map_s);
-      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, 8 - kFp8ScorerBlocks, &map_a);
-      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, 1, &map_r);
+      const int tb = p.x.rope_bf16 ? kFp8bRecord : kDqk;
+      const int nch = p.x.rope_bf16 ? 8 : 9;
+      st = make_kv_map_fp8(kv, p.x.P, tb, nch, kFp8ScorerBlocks, &map_s);
+      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, tb, nch, 8 - kFp8ScorerBlocks, &map_a);
+      if (st == MLA_OK) {
+        if (p.x.rope_bf16)  // the RoPE bf16 bytes [528, 656) of each record: 2 chunks
+          st = make_kv_map_fp8(static_cast<const uint8_t*>(kv) + kFp8bRopeOffset, p.x.P, tb, 2, 2, &map_r);
+        else                // the RoPE e4m3 chunk (chunk 8 of the row)
+          st = make_kv_map_fp8(kv, p.x.P, tb, nch, 1, &map_r);
+      }
     } else {
       st = make_kv_map4(kv, p.x.P, 9, &map_s);
       if (st == MLA_OK) st = make_kv_map4(kv, p.x.P, 8, &map_a);
@@ -483,6 +500,7 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
   a.q = static_cast<const uint16_t*>(q);
   a.kv = kv;
   a.kv_scales = kv_scales;
+  a.rope_bf16 = p.x.rope_bf16 ? 1 : 0;
   a.block_table = bt;
   a.seqlens = seqlens;
   a.hdr = reinterpret_cast<const int32_t*>(p.ws + p.lay.header);

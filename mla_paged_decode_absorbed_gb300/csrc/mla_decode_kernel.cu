@@ -65,8 +65,9 @@ constexpr int kRawSlot = 64 * 64;                  // one raw chunk: 64 tokens x
 constexpr int kRawOffS = kSB * kBox;               // scorer: raw chunks 0..kSB-1, then the RoPE chunk
 constexpr int kRawOffA = 0;                        // accumulator: raw chunks kSB..7
 constexpr int kRawBytesS = (kSB + 1) * kRawSlot;
+constexpr int kRawBytesSB = (kSB + 2) * kRawSlot;  // variant B: the RoPE is two chunks of bf16
 constexpr int kRawBytesA = (8 - kSB) * kRawSlot;
-static_assert(kRawOffS + kRawBytesS <= 8 * kBox && kRawOffA + kRawBytesA <= kSB * kBox,
+static_assert(kRawOffS + kRawBytesSB <= 8 * kBox && kRawOffA + kRawBytesA <= kSB * kBox,
               "raw chunks must lie in the region the peer's copy fills");
 static_assert(2 * (kSB + 1) <= 10 && 2 * (8 - kSB) <= 10, "at most 10 pieces per dequant thread");
 constexpr int kPBytes = kRowsPerBlock * 64 * 2;    // P tile: 128 rows x 64 keys, SW128 K-major
@@ -441,10 +442,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 // the peer's converted blocks will complete on kv_full
                 mbar_arrive_expect_tx(smem_u32(&bars->kv_full[stage]),
                                       static_cast<uint32_t>(scorer ? (8 - kSB) * kBox : kSB * kBox));
-                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(scorer ? kRawBytesS : kRawBytesA));
+                mbar_arrive_expect_tx(
+                    fb, static_cast<uint32_t>(scorer ? (a.rope_bf16 ? kRawBytesSB : kRawBytesS) : kRawBytesA));
                 if (scorer) {
                   tma_load_4d(smem_u32(dst + kRawOffS), &kv_map_s, 0, 0, 0, pid, fb);
-                  tma_load_4d(smem_u32(dst + kRawOffS + kSB * kRawSlot), &kv_map_r, 0, 0, 8, pid, fb);
+                  // the RoPE: chunk 8 of an e4m3 row, or the two bf16 chunks of a variant B record
+                  tma_load_4d(smem_u32(dst + kRawOffS + kSB * kRawSlot), &kv_map_r, 0, 0, a.rope_bf16 ? 0 : 8, pid, fb);
                 } else {
                   tma_load_4d(smem_u32(dst + kRawOffA), &kv_map_a, 0, 0, kSB, pid, fb);
                 }
@@ -1167,6 +1170,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t send_bytes = static_cast<uint32_t>(scorer ? kSB * kBox : (8 - kSB) * kBox);
     const int peer_stage_bytes = scorer ? kStageO : kStageS;
     const uint32_t peer_smem = mapa_shared(smem_u32(smem), peer);
+    const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(a.kv);
+    const bool rope_b = a.rope_bf16 != 0;  // variant B: scales in the record, RoPE in bf16
     SegIter it = it0;
     Seg s;
     int stage = 0;
@@ -1186,9 +1191,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         const bool live = !bad && t < seqlen - p * kPage;
         float s_lo = 0.f, s_hi = 0.f;
         if (live) {
-          const float* sp = a.kv_scales + (static_cast<size_t>(pid) * kPage + t) * kGroups;
-          s_lo = __ldg(sp + g_lo);
-          s_hi = __ldg(sp + g_hi);
+          const size_t row = static_cast<size_t>(pid) * kPage + t;
+          if (rope_b) {  // four latent scales in the record (the RoPE has none)
+            const float* sp = reinterpret_cast<const float*>(kv8 + row * kFp8bRecord + kFp8bScaleOffset);
+            s_lo = __ldg(sp + min(g_lo, 3));
+            s_hi = __ldg(sp + min(g_hi, 3));
+          } else {
+            const float* sp = a.kv_scales + row * kGroups;
+            s_lo = __ldg(sp + g_lo);
+            s_hi = __ldg(sp + g_hi);
+          }
         }
         // our blocks of this stage were copied to the peer three pages ago:
         // reuse them only after the peer's MMAs are done with that page
@@ -1200,7 +1212,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           ok = false;
           break;
         }
-        const bool out_of_range = live && !(fmaxf(fabsf(s_lo), fabsf(s_hi)) * 448.f <= 65504.f);
+        bool out_of_range = live && !(fmaxf(fabsf(s_lo), fabsf(s_hi)) * 448.f <= 65504.f);
         const __half hl = __float2half_rn(s_lo), hh = __float2half_rn(s_hi);
         const __half ll = __float2half_rn(s_lo - __half2float(hl)), lh = __float2half_rn(s_hi - __half2float(hh));
         uint8_t* const dst = smem + stage * stage_bytes;
@@ -1212,7 +1224,26 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             const int f = n * h + i;
             const int c = piece_ch(f);
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (live) {
+            if (live && rope_b && c >= kDv) {
+              // variant B RoPE piece: 16 bf16 channels (two 16-byte granules of
+              // the two RoPE chunks) -> fp16, exact inside the fp16 range
+              const int qr = f & 3;
+              const uint8_t* rr = raw + (kSB + (qr >> 1)) * kRawSlot;
+              const uint4 r0 = *reinterpret_cast<const uint4*>(rr + (((2 * (qr & 1)) ^ rsw) << 4));
+              const uint4 r1 = *reinterpret_cast<const uint4*>(rr + (((2 * (qr & 1) + 1) ^ rsw) << 4));
+              const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+              uint32_t hw[8];
+              float amax = 0.f;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
+                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                hw[k] = pack_f16x2(lo, hi);
+              }
+              out_of_range |= !(amax <= 65504.f);
+              o0 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              o1 = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            } else if (live) {
               const uint4 r = *reinterpret_cast<const uint4*>(raw + (f >> 2) * kRawSlot + (((f & 3) ^ rsw) << 4));
               const bool lo = group_of(c) == g_lo;
               const __half2 shi = __half2half2(lo ? hl : hh), slo = __half2half2(lo ? ll : lh);

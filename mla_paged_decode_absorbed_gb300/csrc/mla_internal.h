@@ -13,6 +13,8 @@ constexpr int kDv = 512;             // output channels (latent part of a KV row
 constexpr int kRowsPerBlock = 128;   // query rows (token-major (i, h)) per work unit = MMA M
 constexpr int kGroups = 5;           // fp8 scale groups per token
 constexpr int kFp8ScorerBlocks = 3;  // fp8: latent 64-channel blocks the scorer converts (rest: accumulator)
+constexpr int kFp8bRecord = 656;     // fp8 variant B bytes per token: e4m3 latent, 4 fp32 scales, RoPE bf16
+constexpr int kFp8bScaleOffset = 512, kFp8bRopeOffset = 528;
 constexpr int kDefaultOverhead = 2;  // planner cost per work unit, in pages
 // A split unit with at most this many pieces is merged inside the attention
 // kernel by the piece that finishes last; units with more pieces are merged by
@@ -31,7 +33,7 @@ enum : int { kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters 
 struct DecodeArgs {
   const uint16_t* q;          // bf16 [B, s_q, H, 576]
   const void* kv;             // the cache itself (the fp8 variant reads it with plain loads)
-  const float* kv_scales;     // fp32 [P, 64, 5] (fp8 cache) or nullptr
+  const float* kv_scales;     // fp32 [P, 64, 5] (fp8 variant A) or nullptr
   const int32_t* block_table; // [B, max_pages]
   const int32_t* seqlens;     // [B]
   const int32_t* hdr;         // workspace header
@@ -46,6 +48,7 @@ struct DecodeArgs {
   int32_t* err;               // workspace word 0
   int B, s_q, H, R, n_rb, U, num_pages, max_pages, overhead;
   float scale_log2;           // softmax_scale * log2(e)
+  int rope_bf16;              // fp8 variant B: 656-byte token records, scales inside, RoPE in bf16
 };
 
 struct CombineArgs {

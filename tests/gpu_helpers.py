@@ -24,7 +24,8 @@ def to_device(inp, device="cuda"):
 def run_gpu(inp, max_clusters: int = 0, plan_overhead: int = 0, decoder=None, tensors=None):
     """out [rows, 512] float64, lse [rows] float64, device status, decoder."""
     dec = decoder or mla.MlaDecoder(inp.batch, inp.s_q, inp.heads, inp.num_pages, inp.max_pages_per_seq,
-                                    kv_fp8=inp.kv_fp8, max_clusters=max_clusters, plan_overhead=plan_overhead)
+                                    kv_fp8=inp.kv_fp8, max_clusters=max_clusters, plan_overhead=plan_overhead,
+                                    rope_bf16=inp.rope_bf16)
     q, kv, sc, bt, sl = tensors or to_device(inp)
     out, lse = dec(q, kv, bt, sl, inp.softmax_scale, kv_scales=sc)
     torch.cuda.synchronize()
@@ -41,10 +42,17 @@ def fp16_k_lse_shift(inp, rows=None):
     by running the oracle twice on fp64 caches built here with torch (the
     exact product and its fp16 rounding); nothing comes from the CUDA path."""
     import oracle
-    codes = inp.kv.view(torch.float8_e4m3fn).to(torch.float64)
-    sc = inp.kv_scales.to(torch.float64)
-    grp = torch.tensor([0] * 128 + [1] * 128 + [2] * 128 + [3] * 128 + [4] * 64)
-    exact = codes * sc[:, :, grp]
+    if getattr(inp, "rope_bf16", False):  # variant B records
+        rec = inp.kv
+        lat = rec[:, :, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        sc4 = rec[:, :, 512:528].contiguous().view(torch.float32).to(torch.float64)
+        rope = rec[:, :, 528:].contiguous().view(torch.bfloat16).to(torch.float64)
+        exact = torch.cat([lat * sc4.repeat_interleave(128, dim=-1), rope], dim=-1)
+    else:
+        codes = inp.kv.view(torch.float8_e4m3fn).to(torch.float64)
+        sc = inp.kv_scales.to(torch.float64)
+        grp = torch.tensor([0] * 128 + [1] * 128 + [2] * 128 + [3] * 128 + [4] * 64)
+        exact = codes * sc[:, :, grp]
     rounded = exact.to(torch.float16).to(torch.float64)
     q = inp.q.to(torch.float64)
     _, l_ex = oracle.mla_decode(q, exact, inp.block_table, inp.seqlens, inp.s_q, inp.softmax_scale,

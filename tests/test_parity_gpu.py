@@ -61,12 +61,13 @@ def test_tiny_workload_every_output():
     ("mtp", dict(batch=2)),
     ("long", dict(seqlens=[20000, 3000, 64, 700])),
     ("fp8", dict(batch=3)),
+    ("fp8b", dict(batch=3)),
 ])
 def test_reduced_workloads_every_output(name, kw):
     _check(gen.make_inputs(name, **kw))
 
 
-@pytest.mark.parametrize("name", ["decode", "mtp", "long", "fp8", "mtp6"])
+@pytest.mark.parametrize("name", ["decode", "mtp", "long", "fp8", "mtp6", "fp8b"])
 def test_full_size_workloads_sampled_rows(name):
     inp = gen.make_inputs(name)
     rows = gen.sample_rows(inp, 160)
@@ -100,6 +101,31 @@ def test_forced_splits_match(clusters, ovh, fp8):
 ])
 def test_edge_shapes(seqlens, heads, s_q, fp8):
     _check(gen.make_inputs("x", seqlens=seqlens, heads=heads, s_q=s_q, kv_fp8=fp8, seed=sum(seqlens) + heads))
+
+
+@pytest.mark.parametrize("seqlens,heads,s_q,clusters", [
+    ([65, 3, 128], 16, 1, 0),            # tails and a 3-key request
+    ([1], 4, 1, 0),                      # a single key (lse is that key's score)
+    ([2000, 5, 130], 128, 6, 0),         # five draft tokens, a request shorter than s_q
+    ([1000, 64, 1, 2500, 130], 32, 2, 3),  # many segments per cluster, split units merged
+])
+def test_fp8_variant_b(seqlens, heads, s_q, clusters):
+    """fp8 variant B: 656-byte token records (e4m3 latent with four scales
+    inside the record, RoPE kept in bf16)."""
+    inp = gen.make_inputs("x", seqlens=seqlens, heads=heads, s_q=s_q, kv_fp8=True, rope_bf16=True,
+                          seed=sum(seqlens) + heads + 5)
+    _check(inp, max_clusters=clusters)
+
+
+def test_fp8_variant_b_bad_page_is_reported():
+    inp = gen.make_inputs("x", seqlens=[300, 50], heads=16, s_q=1, kv_fp8=True, rope_bf16=True, seed=4)
+    inp.block_table[0, 2] = inp.num_pages + 5
+    out_g, lse_g, status, _ = run_gpu(inp)
+    assert status == mla.MLA_ERR_DEVICE_BOUNDS
+    assert np.isfinite(out_g).all()
+    out_r, lse_r = oracle.mla_decode(inp.q[1:], inp.kv, inp.block_table[1:], inp.seqlens[1:], 1, inp.softmax_scale,
+                                     kv_dtype=oracle.KV_FP8B)
+    compare(out_g[16:], lse_g[16:], out_r, lse_r, TOL_FP8)
 
 
 def test_full_pool_no_spare_and_max_pages():
