@@ -283,7 +283,9 @@ __device__ __forceinline__ float max64(const float (&x)[64]) {
   return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
-template <bool kFp8>
+// kRopeB (with kFp8): fp8 variant B, 656-byte token records (scales inside,
+// RoPE in bf16).
+template <bool kFp8, bool kRopeB = false>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map_s, const __grid_constant__ CUtensorMap kv_map_a,
                       const __grid_constant__ CUtensorMap kv_map_r,
@@ -443,11 +445,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 mbar_arrive_expect_tx(smem_u32(&bars->kv_full[stage]),
                                       static_cast<uint32_t>(scorer ? (8 - kSB) * kBox : kSB * kBox));
                 mbar_arrive_expect_tx(
-                    fb, static_cast<uint32_t>(scorer ? (a.rope_bf16 ? kRawBytesSB : kRawBytesS) : kRawBytesA));
+                    fb, static_cast<uint32_t>(scorer ? (kRopeB ? kRawBytesSB : kRawBytesS) : kRawBytesA));
                 if (scorer) {
                   tma_load_4d(smem_u32(dst + kRawOffS), &kv_map_s, 0, 0, 0, pid, fb);
                   // the RoPE: chunk 8 of an e4m3 row, or the two bf16 chunks of a variant B record
-                  tma_load_4d(smem_u32(dst + kRawOffS + kSB * kRawSlot), &kv_map_r, 0, 0, a.rope_bf16 ? 0 : 8, pid, fb);
+                  tma_load_4d(smem_u32(dst + kRawOffS + kSB * kRawSlot), &kv_map_r, 0, 0, kRopeB ? 0 : 8, pid, fb);
                 } else {
                   tma_load_4d(smem_u32(dst + kRawOffA), &kv_map_a, 0, 0, kSB, pid, fb);
                 }
@@ -1171,7 +1173,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const int peer_stage_bytes = scorer ? kStageO : kStageS;
     const uint32_t peer_smem = mapa_shared(smem_u32(smem), peer);
     const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(a.kv);
-    const bool rope_b = a.rope_bf16 != 0;  // variant B: scales in the record, RoPE in bf16
     SegIter it = it0;
     Seg s;
     int stage = 0;
@@ -1192,7 +1193,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         float s_lo = 0.f, s_hi = 0.f;
         if (live) {
           const size_t row = static_cast<size_t>(pid) * kPage + t;
-          if (rope_b) {  // four latent scales in the record (the RoPE has none)
+          if (kRopeB) {  // four latent scales in the record (the RoPE has none)
             const float* sp = reinterpret_cast<const float*>(kv8 + row * kFp8bRecord + kFp8bScaleOffset);
             s_lo = __ldg(sp + min(g_lo, 3));
             s_hi = __ldg(sp + min(g_hi, 3));
@@ -1224,7 +1225,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             const int f = n * h + i;
             const int c = piece_ch(f);
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (live && rope_b && c >= kDv) {
+            if (kRopeB && live && c >= kDv) {
               // variant B RoPE piece: 16 bf16 channels (two 16-byte granules of
               // the two RoPE chunks) -> fp16, exact inside the fp16 range
               const int qr = f & 3;
@@ -1331,7 +1332,12 @@ static cudaLaunchConfig_t make_cfg(bool fp8, int clusters, cudaStream_t stream, 
 }
 
 static cudaError_t set_smem_attr(bool fp8) {
-  if (fp8) return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (fp8) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mla_decode_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  }
   return cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
 }
 
@@ -1340,7 +1346,8 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters) {
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_cfg(fp8, 1, nullptr, attr);
-  if (fp8) return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<true>, &cfg);
+  // both fp8 variants have the same block size and shared memory
+  if (fp8) return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<true, false>, &cfg);
   return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<false>, &cfg);
 }
 
@@ -1351,8 +1358,12 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map_s, cons
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_cfg(fp8, clusters, stream, attr, true);
+  if (fp8 && a.rope_bf16)
+    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, true>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map,
+                              out_map4, a);
   if (fp8)
-    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map, out_map4, a);
+    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, false>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map,
+                              out_map4, a);
   return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map, out_map4, a);
 }
 
