@@ -234,7 +234,11 @@ const char* mla_status_string(int status);
 /* Byte offsets of the workspace regions (for tests and tools that inspect the
  * plan).  The header is int32 words: [0] error bits, [1] W, [2] total cost,
  * [3] units, [4] clusters, [5] plan overhead, [6] number of units of more
- * than three pieces (the combine jobs of mla_combine()).  cl_first is int32 [clusters] (first
+ * than three pieces (the combine jobs of mla_combine()), [7] stall request:
+ * mla_plan() writes 0; a nonzero value written there afterwards makes the next
+ * mla_decode_attention() wait on a barrier that nothing signals, so its
+ * bounded pipeline wait runs out and it reports MLA_ERR_DEVICE_TIMEOUT (for
+ * testing the timeout path without a fault).  cl_first is int32 [clusters] (first
  * unit each cluster touches), pre is int32 [units + 1] (cost prefix), sync is
  * int32 [8*clusters]: merge counters [clusters] and partial-slot ready flags
  * [2*clusters] (mla_plan() clears them and every completed attention kernel

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
   const int lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     hdr[kHdrErr] = 0;
+    hdr[kHdrStall] = 0;
     s_njobs = 0;
   }
   for (int i = tid; i < 4 * G; i += T) sync[i] = 0;

@@ -85,7 +85,7 @@ constexpr int kOffAlpha = kOffP + 2 * kPBytes;     // accumulator: rescale facto
 constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: (row sum, lse) [128]
 constexpr int kAccEnd = kOffL + kRowsPerBlock * 8;
 constexpr int kOffBars = kScorerEnd > kAccEnd ? kScorerEnd : kAccEnd;
-constexpr int kBarBytes = 320;
+constexpr int kBarBytes = 384;
 constexpr int kSmemMax = 232448;
 constexpr int kSmem = kSmemMax;                    // layout + slack for aligning the base
 constexpr int kAlignSlack = kSmem - kOffBars - kBarBytes;
@@ -130,6 +130,7 @@ struct Bars {
   uint64_t dq_sync;              // fp8: the dequant threads wrote their blocks (128), bounded
   uint64_t peer_empty[kStages];  // fp8: the peer's MMAs finished the stage (peer's multicast commit)
   uint64_t raw_free[kStages];    // fp8: the peer read its raw chunks, our copy may land (remote, 1)
+  uint64_t stall;                // never signalled: the wait a test's stall request runs out on
   int abort_flag;
   uint32_t tmem_base;
   int ticket;             // accumulator: finish order of this piece among its unit's pieces
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(smem_u32(&bars->peer_empty[s]), 1);
       mbar_init(smem_u32(&bars->raw_free[s]), 1);
     }
+    mbar_init(smem_u32(&bars->stall), 1);
     mbar_init(smem_u32(&bars->dq_sync), 128);
     bars->abort_flag = 0;
     fence_mbarrier_init_cluster();
@@ -496,6 +498,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     uint32_t ph = 0, q_ph = 0, ofree_ph = 0;
     uint32_t t = 0;  // tile counter over the whole kernel
     bool ok = true;
+    if (scorer && __ldg(a.hdr + kHdrStall) != 0) {
+      // a test's stall request: wait on a barrier nothing signals, so the
+      // bounded wait runs out and the whole cluster takes its abort path
+      if (!mbar_wait(smem_u32(&bars->stall), 0u, abort_flag)) ok = false;
+    }
     if (scorer) {
       // S[b] = Q K^T: 36 steps of K=16 over the 576 channels, A = Q in TMEM.
       const uint32_t idesc = idesc_f16_f32(128, 64, false, false, !kFp8);

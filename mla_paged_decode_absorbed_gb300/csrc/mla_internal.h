@@ -28,7 +28,11 @@ enum : int32_t { kErrBounds = 1, kErrTimeout = 2, kErrRange = 4 };
 
 // Workspace header words (int32).
 // kHdrCombine: number of units with more than kFuseMax pieces (combine jobs).
-enum : int { kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters = 4, kHdrOvh = 5, kHdrCombine = 6 };
+// kHdrStall: a test writes nonzero here after the plan to make the next
+// attention kernel's scorers wait on a barrier nothing signals (the plan clears it).
+enum : int {
+  kHdrErr = 0, kHdrW = 1, kHdrTotal = 2, kHdrUnits = 3, kHdrClusters = 4, kHdrOvh = 5, kHdrCombine = 6, kHdrStall = 7
+};
 
 struct DecodeArgs {
   const uint16_t* q;          // bf16 [B, s_q, H, 576]

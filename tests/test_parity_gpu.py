@@ -342,3 +342,35 @@ def test_attention_rerun_without_replanning():
     out_r, lse_r = oracle.mla_decode_inputs(inp)
     compare(outs[0][0].float().cpu().numpy().reshape(-1, 512).astype(np.float64),
             outs[0][1].cpu().numpy().reshape(-1).astype(np.float64), out_r, lse_r, TOL_BF16)
+
+
+# ------------------------------------------------------------------ timeout path
+@pytest.mark.parametrize("fp8", [False, True])
+def test_pipeline_timeout_is_reported_and_the_context_stays_usable(fp8):
+    """A stall request (workspace header word 7, written after the plan) makes
+    every scorer wait on a barrier nothing signals.  The bounded wait runs out
+    (about a second), both CTAs of every cluster take the abort path and tear
+    down, the call reports MLA_ERR_DEVICE_TIMEOUT, and the next call on the
+    same context (whose plan clears the request) is correct.  No fault, trap
+    or unbounded wait is involved."""
+    import time
+    inp = gen.make_inputs("x", seqlens=[700, 300], heads=16, s_q=1, kv_fp8=fp8, seed=12)
+    t = to_device(inp)
+    q, kv, sc, bt, sl = t
+    d = mla.make_desc(inp.batch, 1, 16, inp.num_pages, inp.max_pages_per_seq, kv_fp8=fp8)
+    ws = mla.alloc_workspace(d)
+    lay = mla.mla_get_workspace_layout(d, mla.mla_num_clusters(d))
+    out = torch.zeros((inp.batch, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((inp.batch, 1, 16), dtype=torch.float32, device="cuda")
+    mla.mla_plan(d, sl, ws)
+    ws[lay.header + 28:lay.header + 32].view(torch.int32).fill_(1)
+    t0 = time.monotonic()
+    mla.mla_decode_attention(d, q, kv, sc, bt, sl, 1, inp.softmax_scale, out, lse, ws)
+    mla.mla_combine(d, out, lse, ws)
+    assert mla.mla_get_device_error(ws) == mla.MLA_ERR_DEVICE_TIMEOUT
+    assert time.monotonic() - t0 < 30
+    out_g, lse_g, status, dec = run_gpu(inp, tensors=t)
+    assert status == mla.MLA_OK
+    out_r, lse_r = oracle.mla_decode_inputs(inp)
+    compare(out_g, lse_g, out_r, lse_r, TOL_FP8 if fp8 else TOL_BF16,
+            lse_extra=fp16_k_lse_shift(inp) if fp8 else None)
