@@ -36,7 +36,7 @@ enum : int {
 
 struct DecodeArgs {
   const uint16_t* q;          // bf16 [B, s_q, H, 576]
-  const void* kv;             // the cache itself (the fp8 variant reads it with plain loads)
+  const void* kv;             // the cache (fp8 variant B: its records' scales are read with plain loads)
   const float* kv_scales;     // fp32 [P, 64, 5] (fp8 variant A) or nullptr
   const int32_t* block_table; // [B, max_pages]
   const int32_t* seqlens;     // [B]
