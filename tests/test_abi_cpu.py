@@ -200,3 +200,19 @@ def test_absorption_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert lib.mla_project_out(A, A, 0, 4, A, None, None) == bad
     assert lib.mla_project_out(A, None, 3, 4, A, None, None) == bad
     assert lib.mla_project_out(A, A, 3, 4, A + 2, None, None) == bad
+
+
+def test_fp8_variant_b_descriptor_and_arguments(lib):
+    """fp8 variant B (656-byte records, scales inside): a valid descriptor
+    sizes a workspace like the other fp8 layout, kv_scales must be NULL, and
+    the binding refuses the layout without the fp8 cache."""
+    d = _desc(kv_fp8=True, rope_bf16=True)
+    assert d.kv_dtype == mla.MLA_KV_FP8_E4M3_ROPE_BF16
+    assert mla.mla_workspace_size(d, 152) == mla.mla_workspace_size(_desc(kv_fp8=True), 152) > 0
+    ok = 1 << 20
+    assert lib.mla_decode(ctypes.byref(d), ok, ok, ok, ok, ok, 1, 0.07, ok, ok, ok, 1 << 30, None) \
+        == mla.MLA_ERR_INVALID_ARG                             # the scales live in the records
+    assert lib.mla_decode(ctypes.byref(d), ok, ok + 8, None, ok, ok, 1, 0.07, ok, ok, ok, 1 << 30, None) \
+        == mla.MLA_ERR_INVALID_ARG                             # the records must be 16-byte aligned
+    with pytest.raises(ValueError):
+        _desc(rope_bf16=True)
