@@ -17,19 +17,23 @@
  *
  * The split of each request's pages across SMs and the LSE merge of the pieces
  * follow the cache partitioning of the same digest, section 1.4 ("Append
- * Attention 优化", FLAGS_cascade_attention_max_partition_size).
+ * Attention 优化", FLAGS_cascade_attention_max_partition_size).  The two
+ * absorption GEMMs that put q into this form and take the output back to
+ * the head dimension are mla_absorb_q() and mla_project_out().
  *
  * Conventions for every entry point:
  *   - Pointers named as device pointers must point to device memory of the
  *     current CUDA device; the caller owns every buffer, the library allocates
- *     nothing and keeps no state besides a per-device cache of launch limits.
+ *     nothing and keeps no state besides a per-device cache of launch limits
+ *     (and, for mla_decode_noalloc() only, a fixed scratch array of its own).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *     asynchronous on that stream and never synchronise the host, except
  *     mla_get_device_error().
  *   - Problems the host can see (bad sizes, NULL or misaligned pointers, short
  *     workspace) return a negative mla_status and launch nothing.  Problems
  *     only the device can see (a page id outside the pool, a seqlen beyond the
- *     block table, a pipeline wait that timed out) set an error word in the
+ *     block table, an fp8 value outside the fp16 compute range, a pipeline
+ *     wait that timed out) set an error word in the
  *     workspace, the kernels finish without trapping, and
  *     mla_get_device_error() reports them.  Nothing aborts the process.
  */
