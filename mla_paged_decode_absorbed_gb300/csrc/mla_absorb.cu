@@ -34,6 +34,18 @@ constexpr int kGemmThreads = 128;           // warp 0 loads, warp 1 issues MMAs,
 constexpr int kChunkA = 128 * 64 * 2;       // one 64-channel chunk of a 128-row A tile (16 KB)
 constexpr int kNopeDim = 128, kRopeDim = 64, kLat = 512;
 
+constexpr int kMaxStages = 8;
+constexpr int kStageBudget = 200 * 1024;  // shared memory for the operand stages
+
+// Operand stages: absorb has two K chunks (both in flight); project has
+// eight, as many in flight as fit (8 at 64 tokens, 6 at 128, 4 at 256), so
+// that few rounds of load latency are exposed.
+__host__ __device__ constexpr int gemm_stages(bool project, int tt) {
+  return project ? ((kStageBudget / (kChunkA + tt * 128)) < kMaxStages ? (kStageBudget / (kChunkA + tt * 128))
+                                                                         : kMaxStages)
+                 : 2;
+}
+
 struct GemmArgs {
   const uint16_t* rope;  // absorb: q_rope [T, H, 64] (copied into q[..., 512:576]); project: unused
   uint16_t* y;           // output: absorb q [T, H, 576]; project o [T, H, 128]
@@ -54,14 +66,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mla_absorb_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                            const GemmArgs a) {
   constexpr int kChunks = kProject ? kLat / 64 : kNopeDim / 64;  // K in 64-channel chunks
-  constexpr int kStages = kProject ? 3 : 2;
+  const int kStages = gemm_stages(kProject, a.tt);               // all chunks in flight when they fit
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tt = a.tt;
   const int stage_bytes = kChunkA + tt * 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* done = empty + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,7 +193,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 int token_tile(int T) { return T <= 64 ? 64 : (T <= 128 ? 128 : 256); }
 
-int gemm_smem(bool project, int tt) { return (project ? 3 : 2) * (kChunkA + tt * 128) + 1024 + 64; }
+// stages, alignment slack, barriers (2 x kMaxStages + 1 mbarriers and the TMEM address)
+int gemm_smem(bool project, int tt) { return gemm_stages(project, tt) * (kChunkA + tt * 128) + 1024 + 256; }
+static_assert((2 * kMaxStages + 1) * 8 + 4 <= 256, "barrier block");
 
 // bf16 tensor with up to 3 dims (innermost first) as a TMA map with a
 // 64-element x box[1] x box[2] box, 128-byte swizzled.
