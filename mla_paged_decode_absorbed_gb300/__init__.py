@@ -7,8 +7,10 @@ library cannot be loaded the calls raise.
 
 Functions mirror the C entry points: ``mla_workspace_size``, ``mla_plan``,
 ``mla_decode_attention``, ``mla_combine``, ``mla_decode``,
-``mla_get_device_error``.  ``MlaDecoder`` bundles a descriptor and a cached
-workspace for repeated calls.
+``mla_get_device_error``.  Each checks its tensors' dtype, shape, contiguity
+and device against the descriptor before the call (``check_decode_tensors``),
+since the C ABI sees only pointers.  ``MlaDecoder`` bundles a descriptor and
+a cached workspace for repeated calls.
 """
 from __future__ import annotations
 
@@ -169,13 +171,49 @@ def alloc_workspace(desc: MlaDesc, device=None) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def check_decode_tensors(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, out, lse, cuda: bool = True):
+    """Checks a decode call's tensors against the descriptor (dtype, shape,
+    contiguity and, with ``cuda``, the device) and returns ``kv`` as the
+    library reads it (an e4m3 tensor viewed as bytes).  The C ABI sees only
+    pointers, so this is where a tensor too small for the descriptor is
+    caught before a kernel reads past it."""
+    B, sq, H = desc.batch, desc.s_q, desc.num_heads
+    _expect(q, "q", torch.bfloat16, (B, sq, H, D_QK), cuda)
+    if desc.kv_dtype == MLA_KV_FP8_E4M3_ROPE_BF16:
+        _expect(kv, "kv", torch.uint8, (desc.num_pages, PAGE, FP8B_RECORD), cuda)
+        if kv_scales is not None:
+            raise ValueError("fp8 variant B keeps its scales inside the token records")
+    elif desc.kv_dtype == MLA_KV_FP8_E4M3:
+        if isinstance(kv, torch.Tensor) and kv.dtype == torch.float8_e4m3fn:
+            kv = kv.view(torch.uint8)
+        _expect(kv, "kv", torch.uint8, (desc.num_pages, PAGE, D_QK), cuda)
+        _expect(kv_scales, "kv_scales", torch.float32, (desc.num_pages, PAGE, 5), cuda)
+    else:
+        _expect(kv, "kv", torch.bfloat16, (desc.num_pages, PAGE, D_QK), cuda)
+        if kv_scales is not None:
+            raise ValueError("kv_scales is only for the fp8 cache")
+    _expect(block_table, "block_table", torch.int32, (B, desc.max_pages_per_seq), cuda)
+    _expect(seqlens, "seqlens", torch.int32, (B,), cuda)
+    _expect(out, "out", torch.bfloat16, (B, sq, H, D_V), cuda)
+    _expect(lse, "lse", torch.float32, (B, sq, H), cuda)
+    return kv
+
+
+def _check_workspace(desc: MlaDesc, workspace, cuda: bool = True):
+    _expect(workspace, "workspace", torch.uint8, None, cuda)
+
+
 def mla_plan(desc: MlaDesc, seqlens: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    _expect(seqlens, "seqlens", torch.int32, (desc.batch,))
+    _check_workspace(desc, workspace)
     _check(_load().mla_plan(ctypes.byref(desc), _ptr(seqlens), _ptr(workspace), workspace.numel(),
                             _stream(stream)), "mla_plan")
 
 
 def mla_decode_attention(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, softmax_scale: float,
                          out, lse, workspace, stream=None) -> None:
+    kv = check_decode_tensors(desc, q, kv, kv_scales, block_table, seqlens, out, lse)
+    _check_workspace(desc, workspace)
     _check(_load().mla_decode_attention(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table),
                                         _ptr(seqlens), int(s_q), float(softmax_scale), _ptr(out), _ptr(lse),
                                         _ptr(workspace), workspace.numel(), _stream(stream)),
@@ -183,13 +221,18 @@ def mla_decode_attention(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, 
 
 
 def mla_combine(desc: MlaDesc, out, lse, workspace, stream=None) -> None:
+    _expect(out, "out", torch.bfloat16, (desc.batch, desc.s_q, desc.num_heads, D_V))
+    _expect(lse, "lse", torch.float32, (desc.batch, desc.s_q, desc.num_heads))
+    _check_workspace(desc, workspace)
     _check(_load().mla_combine(ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                _stream(stream)), "mla_combine")
 
 
 def mla_decode(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, softmax_scale: float, out, lse,
                workspace, stream=None) -> None:
-    """Raw call of the C ``mla_decode`` on caller-provided tensors."""
+    """The C ``mla_decode`` on caller-provided tensors (checked against the descriptor)."""
+    kv = check_decode_tensors(desc, q, kv, kv_scales, block_table, seqlens, out, lse)
+    _check_workspace(desc, workspace)
     _check(_load().mla_decode(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table),
                               _ptr(seqlens), int(s_q), float(softmax_scale), _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel(), _stream(stream)), "mla_decode")
@@ -222,8 +265,10 @@ def mla_get_device_error(workspace: torch.Tensor, stream=None) -> int:
     return int(_load().mla_get_device_error(_ptr(workspace), _stream(stream)))
 
 
-def _expect(t: torch.Tensor, name: str, dtype, shape=None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+def _expect(t: torch.Tensor, name: str, dtype, shape=None, cuda: bool = True):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
+    if cuda and not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
@@ -252,28 +297,11 @@ class MlaDecoder:
                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
         d = self.desc
         B, sq, H = d.batch, d.s_q, d.num_heads
-        _expect(q, "q", torch.bfloat16, (B, sq, H, D_QK))
-        if d.kv_dtype == MLA_KV_FP8_E4M3_ROPE_BF16:
-            _expect(kv, "kv", torch.uint8, (d.num_pages, PAGE, FP8B_RECORD))
-            if kv_scales is not None:
-                raise ValueError("fp8 variant B keeps its scales inside the token records")
-        elif d.kv_dtype == MLA_KV_FP8_E4M3:
-            if kv.dtype == torch.float8_e4m3fn:
-                kv = kv.view(torch.uint8)
-            _expect(kv, "kv", torch.uint8, (d.num_pages, PAGE, D_QK))
-            _expect(kv_scales, "kv_scales", torch.float32, (d.num_pages, PAGE, 5))
-        else:
-            _expect(kv, "kv", torch.bfloat16, (d.num_pages, PAGE, D_QK))
-            if kv_scales is not None:
-                raise ValueError("kv_scales is only for the fp8 cache")
-        _expect(block_table, "block_table", torch.int32, (B, d.max_pages_per_seq))
-        _expect(seqlens, "seqlens", torch.int32, (B,))
+        dev = q.device if isinstance(q, torch.Tensor) else self.device
         if out is None:
-            out = torch.empty((B, sq, H, D_V), dtype=torch.bfloat16, device=q.device)
+            out = torch.empty((B, sq, H, D_V), dtype=torch.bfloat16, device=dev)
         if lse is None:
-            lse = torch.empty((B, sq, H), dtype=torch.float32, device=q.device)
-        _expect(out, "out", torch.bfloat16, (B, sq, H, D_V))
-        _expect(lse, "lse", torch.float32, (B, sq, H))
+            lse = torch.empty((B, sq, H), dtype=torch.float32, device=dev)
         mla_decode(d, q, kv, kv_scales, block_table, seqlens, sq, softmax_scale, out, lse, self.workspace, stream)
         return out, lse
 
@@ -296,6 +324,7 @@ def mla_decode_noalloc(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_
     """Raw call of the C ``mla_decode_noalloc`` (scratch inside the library,
     no workspace argument, no device allocation).  Returns the status when
     ``check_device_error`` is set (the call then synchronises the stream)."""
+    kv = check_decode_tensors(desc, q, kv, kv_scales, block_table, seqlens, out, lse)
     st = noalloc_function()(ctypes.byref(desc), _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(block_table), _ptr(seqlens), int(s_q),
             float(softmax_scale), _ptr(out), _ptr(lse), 1 if check_device_error else 0, _stream(stream))
     if st not in (MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_RANGE):
