@@ -117,26 +117,33 @@ class ClockSampler:
         self.device_index = device_index
         self.proc = None
         self.path = None
+        self.out = None
 
     def start(self):
         try:
             import tempfile
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
+            self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
     def stop(self):
         if self.proc is None:
+            if self.out is not None:
+                self.out.close()
+                os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+            self.proc.wait()
+        self.out.close()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
