@@ -36,6 +36,11 @@
  *     wait that timed out) set an error word in the
  *     workspace, the kernels finish without trapping, and
  *     mla_get_device_error() reports them.  Nothing aborts the process.
+ *   - The library sees pointers only: it cannot tell that a buffer is smaller
+ *     than the descriptor says, and a short buffer is read or written past its
+ *     end.  Sizing every buffer as documented below is the caller's part (the
+ *     Python binding checks each tensor's dtype, shape and contiguity against
+ *     the descriptor before the call).
  */
 #ifndef MLA_GB300_H_
 #define MLA_GB300_H_
