@@ -136,6 +136,28 @@ def test_identical_scores_give_mean_of_values():
         assert lse[h] == pytest.approx(s + math.log(n), abs=1e-12)
 
 
+@pytest.mark.parametrize("shift", [1.0e4, -1.0e4])
+def test_common_score_shift_leaves_out_and_moves_lse(shift):
+    """Adding the same amount to every key's score (through a RoPE channel
+    equal for all keys) leaves the softmax weights, and so out, unchanged and
+    moves lse by exactly that amount.  At +-1e4 a softmax without the maximum
+    subtracted overflows (or underflows to 0/0) in fp64, so this also fails
+    if the oracle's stabilisation is missing or wrong."""
+    rng = np.random.default_rng(21)
+    n = 230
+    bt = np.array([[3, 0, 4, 1]], dtype=np.int32)
+    kv = rng.standard_normal((5, 64, 576))
+    kv[:, :, 575] = 1.0
+    q = rng.standard_normal((1, 1, 3, 576))
+    q[..., 575] = 0.0
+    o0, l0 = oracle.mla_decode(q, kv, bt, np.array([n], np.int32), 1, SCALE, kv_dtype=KV_F64)
+    q[..., 575] = shift / SCALE
+    o1, l1 = oracle.mla_decode(q, kv, bt, np.array([n], np.int32), 1, SCALE, kv_dtype=KV_F64)
+    assert np.isfinite(o1).all() and np.isfinite(l1).all()
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0 + shift, rtol=0, atol=1e-9)
+
+
 def test_two_key_hand_derivation():
     """Scores 0 and 1 (scale 1): p = (1, e)/(1+e), lse = ln(1+e)."""
     q = np.zeros((1, 1, 1, 576))
