@@ -283,9 +283,54 @@ def absorption_gemms(inp, flush, hbm_gbs, tflops_peak, iters: int = 10):
     return res
 
 
+def cpu_model() -> str:
+    """CPU model of this host: lscpu's model name (Arm hosts have no model
+    name in /proc/cpuinfo), else /proc/cpuinfo, else the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_one_core(name: str, **kw):
+    """The oracle on one host core over every row of a small workload: GFLOP/s."""
+    import oracle
+    inp = gen.make_inputs(name, **kw)
+    flops, _ = work_of(inp)
+    oracle.set_num_threads(1)
+    try:
+        oracle.mla_decode_inputs(inp)          # warm caches and the library
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.mla_decode_inputs(inp)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 1.0 or reps >= 50:
+                break
+    finally:
+        oracle.set_num_threads(os.cpu_count() or 1)
+    return {"gflops": reps * flops / dt / 1e9, "seconds_per_call": dt / reps, "gflop_per_call": flops / 1e9}
+
+
 def cpu_baseline(inp, seconds: float = 12.0):
     """Time the oracle on a bounded sample of the workload (rank 0, N=1):
-    about `seconds` of host work; a sample smaller than that is repeated."""
+    about `seconds` of host work on all cores; a sample smaller than that is
+    repeated.  Also the oracle on ONE core over every row of the tiny workload
+    and of a four-request cut of the decode workload, and the CPU model."""
     import oracle
     R = inp.s_q * inp.heads
     rows_t, flops, nreq = oracle_sample(inp, seconds)
@@ -296,8 +341,93 @@ def cpu_baseline(inp, seconds: float = 12.0):
         dt = time.perf_counter() - t0
         if dt >= 0.8 * seconds or reps >= 20:
             break
-    return {"value": reps * flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{nreq} of {inp.batch} requests x {R} rows ({flops/1e9:.2f} GFLOP), run {reps}x in {dt:.1f} s"}
+    cores = oracle.num_threads()
+    per_core = {"tiny (every row)": oracle_one_core("tiny"),
+                "decode B=4 (every row)": oracle_one_core("decode", batch=4)}
+    return {"value": reps * flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nreq} of {inp.batch} requests x {R} rows ({flops/1e9:.2f} GFLOP), run {reps}x in {dt:.1f} s",
+            "cpu_model": cpu_model(), "one_core": per_core}
+
+
+def roofline_of(inp, flops, kv_bytes, kms, hbm_gbs, tflops_peak, peak_src, workload):
+    """Roofline entry of the attention kernel: HBM-bound (cache bytes / HBM
+    peak) or tensor-bound (flops / dense 16-bit tensor peak), whichever takes
+    longer at the measured peaks."""
+    name = "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>"
+    if kv_bytes / (hbm_gbs * 1e9) >= flops / (tflops_peak * 1e12):
+        ach = kv_bytes / (kms * 1e-3) / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm_gbs, "unit": "GB/s", "frac": ach / hbm_gbs,
+                "traffic": measured_traffic(workload), "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
+                "algorithmic_bytes_per_launch": kv_bytes}
+    ach = flops / (kms * 1e-3) / 1e12
+    return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tflops_peak, "unit": "TFLOP/s",
+            "frac": ach / tflops_peak, "traffic": measured_traffic(workload),
+            "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone; fp16 has the same dense rate)",
+            "algorithmic_flops_per_launch": flops}
+
+
+def time_workload(mla, inp, dev, stream, flush, steps, warmup, clock_dev, sync_ranks):
+    """Device-resident inputs of `inp`, W warm-up steps, then K timed steps
+    (events around each step on the launching stream, L2 flushed between
+    steps outside the events), then the attention kernel alone in a second
+    loop of the same steps.  Clocks are sampled over both loops."""
+    q = inp.q.to(dev)
+    kv = inp.kv.to(dev)
+    sc = inp.kv_scales.to(dev) if inp.kv_scales is not None else None
+    bt = inp.block_table.to(dev)
+    sl = inp.seqlens.to(dev)
+    dec = mla.MlaDecoder(inp.batch, inp.s_q, inp.heads, inp.num_pages, inp.max_pages_per_seq, kv_fp8=inp.kv_fp8,
+                         rope_bf16=inp.rope_bf16, device=dev)
+    d, ws = dec.desc, dec.workspace
+    out = torch.empty((inp.batch, inp.s_q, inp.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((inp.batch, inp.s_q, inp.heads), dtype=torch.float32, device=dev)
+
+    def step(ev_a=None, ev_b=None):
+        # The three kernels chain by programmatic dependent launch; events
+        # between them (kernel timing) serialise the launches, so the step
+        # loop runs without them and the kernel loop with them.
+        mla.mla_plan(d, sl, ws, stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        mla.mla_decode_attention(d, q, kv, sc, bt, sl, inp.s_q, inp.softmax_scale, out, lse, ws, stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+        mla.mla_combine_workspace(d, out, lse, ws, stream)
+
+    for _ in range(warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = dec.device_error()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device error during warm-up: {mla.status_string(st)}")
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    starts, ends = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    k_a, k_b = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    clocks = ClockSampler(clock_dev)
+    sync_ranks()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        step(k_a[i], k_b[i])
+    torch.cuda.synchronize()
+    sync_ranks()
+    clk = clocks.stop()
+    st = dec.device_error()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device error in the timed steps: {mla.status_string(st)}")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    kms = sum(a.elapsed_time(b) for a, b in zip(k_a, k_b)) / steps
+    return {"ms": ms, "kms": kms, "clocks": clk, "dec": dec, "desc": d, "ws": ws,
+            "tensors": (q, kv, sc, bt, sl, out, lse)}
 
 
 def main():
@@ -309,6 +439,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload map (the other six workloads)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -328,71 +459,17 @@ def main():
     # each replica decodes its own batch of independent requests (weak scaling)
     inp = replica_inputs(args.workload, rank)
     flops, kv_bytes = work_of(inp)
-    q = inp.q.to(dev)
-    kv = inp.kv.to(dev)
-    sc = inp.kv_scales.to(dev) if inp.kv_scales is not None else None
-    bt = inp.block_table.to(dev)
-    sl = inp.seqlens.to(dev)
-    dec = mla.MlaDecoder(inp.batch, inp.s_q, inp.heads, inp.num_pages, inp.max_pages_per_seq, kv_fp8=inp.kv_fp8,
-                         rope_bf16=inp.rope_bf16,
-                         device=dev)
-    d = dec.desc
-    ws = dec.workspace
-    out = torch.empty((inp.batch, inp.s_q, inp.heads, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((inp.batch, inp.s_q, inp.heads), dtype=torch.float32, device=dev)
+    hbm_gbs, tflops_peak, tflops_sust, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step(ev_a=None, ev_b=None):
-        # The three kernels chain by programmatic dependent launch; events
-        # between them (kernel timing) serialise the launches, so the step
-        # loop runs without them and the kernel loop with them.
-        mla.mla_plan(d, sl, ws, stream)
-        if ev_a is not None:
-            ev_a.record(stream)
-        mla.mla_decode_attention(d, q, kv, sc, bt, sl, inp.s_q, inp.softmax_scale, out, lse, ws, stream)
-        if ev_b is not None:
-            ev_b.record(stream)
-        mla.mla_combine(d, out, lse, ws, stream)
-
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    st = dec.device_error()
-    if st != mla.MLA_OK:
-        raise RuntimeError(f"device error during warm-up: {mla.status_string(st)}")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(dev)
-    clocks = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    # the attention kernel alone (events around it), same inputs and flushes
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        step(k_a[i], k_b[i])
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kern_ms = [a.elapsed_time(b) for a, b in zip(k_a, k_b)]
-    ms = sum(step_ms) / len(step_ms)
-    kms = sum(kern_ms) / len(kern_ms)
-    ms, kms = max_over_ranks([ms, kms], dev)
+    clock_dev = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    sync_ranks = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    res = time_workload(mla, inp, dev, stream, flush, args.steps, args.warmup, clock_dev, sync_ranks)
+    ms, kms = max_over_ranks([res["ms"], res["kms"]], dev)
+    dec, d, ws = res["dec"], res["desc"], res["ws"]
+    q, kv, sc, bt, sl, out, lse = res["tensors"]
+    clk = res["clocks"]
 
     # end to end through the C ABI call with host buffers: H2D of the step's
     # inputs (q, block table, seqlens) from pinned memory, decode, D2H of out + lse
@@ -438,23 +515,12 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    hbm_gbs, tflops_peak, tflops_sust, peak_src = load_peaks()
     tflops = world * flops / (ms * 1e-3) / 1e12
     kv_gbs = world * kv_bytes / (ms * 1e-3) / 1e9
     t_roof = max(flops / (tflops_peak * 1e12), kv_bytes / (hbm_gbs * 1e9))
     k_tflops = flops / (kms * 1e-3) / 1e12
     k_gbs = kv_bytes / (kms * 1e-3) / 1e9
-    hbm_bound = kv_bytes / (hbm_gbs * 1e9) >= flops / (tflops_peak * 1e12)
-    if hbm_bound:
-        roof = {"kernel": "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>", "bound": "hbm",
-                "achieved": k_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": k_gbs / hbm_gbs,
-                "traffic": measured_traffic(args.workload), "peak_source": f"{peak_src} hbm_gbs (burst, kernel timed alone)",
-                "algorithmic_bytes_per_launch": kv_bytes}
-    else:
-        roof = {"kernel": "mla_decode_kernel<bf16>" if not inp.kv_fp8 else "mla_decode_kernel<fp8>", "bound": "tensor",
-                "achieved": k_tflops, "peak": tflops_peak, "unit": "TFLOP/s", "frac": k_tflops / tflops_peak,
-                "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
-                "algorithmic_flops_per_launch": flops}
+    roof = roofline_of(inp, flops, kv_bytes, kms, hbm_gbs, tflops_peak, peak_src, args.workload)
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -473,6 +539,26 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     line["absorption_gemms"] = absorption_gemms(inp, flush, hbm_gbs, tflops_peak)
+    if world == 1 and not args.no_workloads:
+        # every other named workload, each in its own launch configuration,
+        # timed the same way (fewer steps), with its own clock record
+        wl = {}
+        for name in gen.WORKLOADS:
+            if name == args.workload:
+                continue
+            w_inp = gen.make_inputs(name)
+            w_flops, w_bytes = work_of(w_inp)
+            r = time_workload(mla, w_inp, dev, stream, flush, min(args.steps, 10), 3, clock_dev, sync_ranks)
+            wl[name] = {
+                "workload": WORKLOAD_TEXT[name], "step_ms": r["ms"], "kernel_ms": r["kms"],
+                "tflops": w_flops / (r["ms"] * 1e-3) / 1e12, "kv_gbs": w_bytes / (r["ms"] * 1e-3) / 1e9,
+                "pct_roofline": max(w_flops / (tflops_peak * 1e12), w_bytes / (hbm_gbs * 1e9)) / (r["ms"] * 1e-3),
+                "roofline": roofline_of(w_inp, w_flops, w_bytes, r["kms"], hbm_gbs, tflops_peak, peak_src, name),
+                "clocks": r["clocks"], "steps": min(args.steps, 10), "warmup": 3,
+            }
+            del r, w_inp
+            torch.cuda.empty_cache()
+        line["workloads"] = wl
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
     print(json.dumps(line), flush=True)

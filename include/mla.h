@@ -107,7 +107,7 @@ int mla_num_clusters(const mla_desc* desc);
 
 /*
  * The whole hot path: mla_plan(), then mla_decode_attention(), then
- * mla_combine(), in order on `stream`.
+ * mla_combine_workspace(), in order on `stream`.
  *
  *   q            device, bf16 [B, s_q, H, 576], contiguous, 16-byte aligned
  *   kv_pages     device, [num_pages, 64, 576] bf16 or e4m3 bytes, or [num_pages, 64, 656] fp8
@@ -147,7 +147,7 @@ mla_status mla_plan(const mla_desc* desc, const int32_t* seqlens, void* workspac
  * output in fp16 with a power-of-two row scale, and its lse) into the
  * workspace; for a unit of two or three pieces the piece that finishes last
  * merges the others' partials with its own result and writes out/lse itself.
- * Units of more pieces are left to mla_combine().  The kernel leaves the
+ * Units of more pieces are left to mla_combine_workspace().  The kernel leaves the
  * workspace's merge counters clear, so it may run again on the same plan;
  * after a device error, run mla_plan() again first.  The kernel is launched
  * as a programmatic dependent of the previous kernel in `stream` (its prologue
@@ -164,11 +164,43 @@ mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void*
  * than three pieces,
  *   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
  * over its pieces, written to out (bf16) and lse.  Needs the plan and the
- * partials of the two previous steps in the same workspace; returns at once
- * on the device when the plan has no such unit.
+ * partials of the two previous steps in the same workspace (the library's
+ * own fp16 partial layout); returns at once on the device when the plan has
+ * no such unit.  To merge partials computed elsewhere, use mla_combine().
  */
-mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                       void* stream);
+mla_status mla_combine_workspace(const mla_desc* desc, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * LSE-weighted merge of split-KV partials that the caller computed (the
+ * cache partitioning of the best-practice digest, section 1.4 "Append
+ * Attention 优化": each request's keys are cut into chunks that are attended
+ * separately and merged afterwards; it is also the merge a split of one
+ * request's keys across devices needs).  For request b, row r < s_q*H, and
+ * its partials k in [split_indptr[b], split_indptr[b+1]):
+ *
+ *   lse[b, r] = ln sum_k exp(lse_part[k, r])                     (natural log)
+ *   out[b, r] = sum_k exp(lse_part[k, r] - lse[b, r]) * o_part[k, r, :]
+ *
+ * A partial with lse_part = -inf saw no key of that row: it contributes
+ * nothing and its o_part row is not read (it may hold anything).  A row with
+ * no contributing partial gets out = 0 and lse = -inf (as mla_decode() does
+ * for a row with no visible key).
+ *
+ *   o_part        device, fp32 [num_partials, s_q*H, 512], contiguous, 16-byte aligned:
+ *                 each partial's normalised output (its own softmax over its keys)
+ *   lse_part      device, fp32 [num_partials, s_q*H], finite or -inf
+ *   split_indptr  device, int32 [B + 1], non-decreasing; indices are clamped to
+ *                 [0, num_partials], so a malformed range reads nothing outside the buffers
+ *   num_partials  >= 0, the first dimension of o_part and lse_part
+ *   out, lse      as mla_decode() (written)
+ *
+ * One kernel, one warp per (request, row), 16-byte coalesced loads and
+ * stores; asynchronous on `stream`; needs no workspace.  Only desc->batch,
+ * s_q and num_heads are used (the rest must still form a valid descriptor).
+ */
+mla_status mla_combine(const mla_desc* desc, const float* o_part, const float* lse_part, const int32_t* split_indptr,
+                       int32_t num_partials, void* out, float* lse, void* stream);
 
 /*
  * Synchronises `stream`, then reads the workspace error word written by the
@@ -196,11 +228,20 @@ mla_status mla_get_device_error(const void* workspace, void* stream);
  * All calls share the array: calls that overlap on the GPU race, so serialise
  * them.  With check_device_error != 0 the call synchronises `stream` and
  * returns the device error status (as mla_get_device_error()); otherwise it
- * returns without synchronising.
+ * returns without synchronising, and mla_noalloc_get_device_error() reads the
+ * status later.
  */
 mla_status mla_decode_noalloc(const mla_desc* desc, const void* q, const void* kv_pages, const float* kv_scales,
                               const int32_t* block_table, const int32_t* seqlens, int32_t s_q, float softmax_scale,
                               void* out, float* lse, int check_device_error, void* stream);
+
+/*
+ * The device error status of the last mla_decode_noalloc() on the current
+ * device (same codes as mla_get_device_error()), for callers that ran it
+ * without check_device_error.  Synchronises `stream` and reads the error word
+ * in the library's scratch array; the next mla_decode_noalloc() clears it.
+ */
+mla_status mla_noalloc_get_device_error(void* stream);
 
 /*
  * Matrix absorption around the attention step (best-practice digest §2.4.3:
@@ -243,7 +284,7 @@ const char* mla_status_string(int status);
 /* Byte offsets of the workspace regions (for tests and tools that inspect the
  * plan).  The header is int32 words: [0] error bits, [1] W, [2] total cost,
  * [3] units, [4] clusters, [5] plan overhead, [6] number of units of more
- * than three pieces (the combine jobs of mla_combine()), [7] stall request:
+ * than three pieces (the combine jobs of mla_combine_workspace()), [7] stall request:
  * mla_plan() writes 0; a nonzero value written there afterwards makes the next
  * mla_decode_attention() wait on a barrier that nothing signals, so its
  * bounded pipeline wait runs out and it reports MLA_ERR_DEVICE_TIMEOUT (for

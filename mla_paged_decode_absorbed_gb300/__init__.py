@@ -6,8 +6,8 @@ device memory and the current stream.  There is no CPU fallback: if the
 library cannot be loaded the calls raise.
 
 Functions mirror the C entry points: ``mla_workspace_size``, ``mla_plan``,
-``mla_decode_attention``, ``mla_combine``, ``mla_decode``,
-``mla_get_device_error``.  Each checks its tensors' dtype, shape, contiguity
+``mla_decode_attention``, ``mla_combine_workspace``, ``mla_combine`` (merge
+of caller-supplied fp32 partials), ``mla_decode``, ``mla_get_device_error``.  Each checks its tensors' dtype, shape, contiguity
 and device against the descriptor before the call (``check_decode_tensors``),
 since the C ABI sees only pointers.  ``MlaDecoder`` bundles a descriptor and
 a cached workspace for repeated calls.
@@ -90,8 +90,10 @@ def _load():
             lib.mla_plan.argtypes = [dp, vp, vp, sz, vp]
             lib.mla_decode_attention.restype = ctypes.c_int
             lib.mla_decode_attention.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+            lib.mla_combine_workspace.restype = ctypes.c_int
+            lib.mla_combine_workspace.argtypes = [dp, vp, vp, vp, sz, vp]
             lib.mla_combine.restype = ctypes.c_int
-            lib.mla_combine.argtypes = [dp, vp, vp, vp, sz, vp]
+            lib.mla_combine.argtypes = [dp, vp, vp, vp, i32, vp, vp, vp]
             lib.mla_decode.restype = ctypes.c_int
             lib.mla_decode.argtypes = [dp, vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp, sz, vp]
             lib.mla_get_device_error.restype = ctypes.c_int
@@ -220,11 +222,30 @@ def mla_decode_attention(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, 
            "mla_decode_attention")
 
 
-def mla_combine(desc: MlaDesc, out, lse, workspace, stream=None) -> None:
+def mla_combine_workspace(desc: MlaDesc, out, lse, workspace, stream=None) -> None:
+    """Step 3 of mla_decode: merges the split pieces a previous
+    mla_decode_attention left in ``workspace``."""
     _expect(out, "out", torch.bfloat16, (desc.batch, desc.s_q, desc.num_heads, D_V))
     _expect(lse, "lse", torch.float32, (desc.batch, desc.s_q, desc.num_heads))
     _check_workspace(desc, workspace)
-    _check(_load().mla_combine(ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+    _check(_load().mla_combine_workspace(ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)), "mla_combine_workspace")
+
+
+def mla_combine(desc: MlaDesc, o_part, lse_part, split_indptr, out, lse, stream=None) -> None:
+    """LSE merge of caller-supplied split-KV partials: ``o_part`` fp32
+    [num_partials, s_q*H, 512], ``lse_part`` fp32 [num_partials, s_q*H],
+    ``split_indptr`` int32 [B+1] (request b owns partials
+    split_indptr[b]..split_indptr[b+1]-1), into ``out`` / ``lse``."""
+    R = desc.s_q * desc.num_heads
+    n = int(o_part.shape[0]) if isinstance(o_part, torch.Tensor) else -1
+    _expect(o_part, "o_part", torch.float32, (n, R, D_V))
+    _expect(lse_part, "lse_part", torch.float32, (n, R))
+    _expect(split_indptr, "split_indptr", torch.int32, (desc.batch + 1,))
+    _expect(out, "out", torch.bfloat16, (desc.batch, desc.s_q, desc.num_heads, D_V))
+    _expect(lse, "lse", torch.float32, (desc.batch, desc.s_q, desc.num_heads))
+    _check(_load().mla_combine(ctypes.byref(desc), _ptr(o_part) if n > 0 else None,
+                               _ptr(lse_part) if n > 0 else None, _ptr(split_indptr), n, _ptr(out), _ptr(lse),
                                _stream(stream)), "mla_combine")
 
 
@@ -317,6 +338,15 @@ def noalloc_function():
                                                                        ctypes.c_void_p, ctypes.c_void_p,
                                                                        ctypes.c_int, ctypes.c_void_p]
     return fn
+
+
+def mla_noalloc_get_device_error(stream=None) -> int:
+    """Device error status of the last mla_decode_noalloc on this device
+    (synchronises the stream)."""
+    fn = _load().mla_noalloc_get_device_error
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p]
+    return int(fn(_stream(stream)))
 
 
 def mla_decode_noalloc(desc: MlaDesc, q, kv, kv_scales, block_table, seqlens, s_q: int, softmax_scale: float,

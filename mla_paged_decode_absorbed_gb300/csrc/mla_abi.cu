@@ -229,6 +229,83 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
 }
 
 
+// ------------------------------------------------------------------ combine of caller partials
+// mla_combine(): the LSE merge of fp32 partials a caller computed.  One warp
+// per (request b, row r): the lanes first reduce the partials' lse maximum,
+// then walk the partials four at a time; lane l owns output channels
+// [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8), so every load instruction of the
+// warp reads 1 KB of one partial row in 16-byte pieces and every store writes
+// 512 contiguous bytes of bf16.  A partial whose lse is -inf is skipped (its
+// row is never read: it may hold anything).
+constexpr int kCpWarps = 8;
+
+__device__ __forceinline__ void fma4(float (&acc)[4], float w, const float4 v) {
+  acc[0] += w * v.x;
+  acc[1] += w * v.y;
+  acc[2] += w * v.z;
+  acc[3] += w * v.w;
+}
+
+__global__ void __launch_bounds__(32 * kCpWarps) mla_combine_partials_kernel(
+    const float* __restrict__ o_part, const float* __restrict__ lse_part, const int32_t* __restrict__ indptr,
+    int num_partials, int R, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.y * kCpWarps + (threadIdx.x >> 5);
+  const int b = blockIdx.x;
+  if (r >= R) return;
+  const int k0 = max(0, __ldg(indptr + b)), k1 = min(num_partials, __ldg(indptr + b + 1));
+  float m = -INFINITY;
+  for (int k = k0 + lane; k < k1; k += 32) m = fmaxf(m, __ldg(lse_part + static_cast<size_t>(k) * R + r));
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  float acc[4][4] = {};  // [lo chunk 0, lo chunk 1, hi chunk 0, hi chunk 1][4]
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int kb = k0; kb < k1; kb += 4) {
+      float w[4];
+      float4 v[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = kb + i;
+        const float l = k < k1 ? __ldg(lse_part + static_cast<size_t>(k) * R + r) : -INFINITY;
+        w[i] = l == -INFINITY ? 0.f : expf(l - m);
+        if (w[i] > 0.f) {
+          const float4* src = reinterpret_cast<const float4*>(o_part + (static_cast<size_t>(k) * R + r) * kDv);
+          v[i][0] = __ldg(src + 2 * lane);
+          v[i][1] = __ldg(src + 2 * lane + 1);
+          v[i][2] = __ldg(src + 64 + 2 * lane);
+          v[i][3] = __ldg(src + 64 + 2 * lane + 1);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[i][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        wsum += w[i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) fma4(acc[j], w[i], v[i][j]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const size_t orow = static_cast<size_t>(b) * R + r;
+  uint4* dst = reinterpret_cast<uint4*>(out + orow * kDv);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float* a2 = acc[2 * h + (q >> 1)];
+      __nv_bfloat162 x = __floats2bfloat162_rn(a2[2 * (q & 1)] * inv, a2[2 * (q & 1) + 1] * inv);
+      pk[q] = *reinterpret_cast<uint32_t*>(&x);
+    }
+    dst[32 * h + lane] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+  if (lane == 0) lse[orow] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
+
 // ------------------------------------------------------------------ host helpers
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -629,8 +706,8 @@ mla_status mla_decode_attention(const mla_desc* desc, const void* q, const void*
                        static_cast<cudaStream_t>(stream));
 }
 
-mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+mla_status mla_combine_workspace(const mla_desc* desc, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   Dims x;
   mla_status st = check_desc(desc, &x);
   if (st != MLA_OK) return st;
@@ -639,6 +716,22 @@ mla_status mla_combine(const mla_desc* desc, void* out, float* lse, void* worksp
   st = prepare(desc, workspace, workspace_bytes, &p);
   if (st != MLA_OK) return st;
   return run_combine(p, out, lse, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_combine(const mla_desc* desc, const float* o_part, const float* lse_part, const int32_t* split_indptr,
+                       int32_t num_partials, void* out, float* lse, void* stream) {
+  Dims x;
+  mla_status st = check_desc(desc, &x);
+  if (st != MLA_OK) return st;
+  if (num_partials < 0 || !split_indptr || !out || !lse || !aligned(split_indptr, 4) || !aligned(out, 16) ||
+      !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (num_partials > 0 && (!o_part || !lse_part || !aligned(o_part, 16) || !aligned(lse_part, 4)))
+    return MLA_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(x.B), static_cast<unsigned>((x.R + kCpWarps - 1) / kCpWarps), 1);
+  mla_combine_partials_kernel<<<grid, 32 * kCpWarps, 0, static_cast<cudaStream_t>(stream)>>>(
+      o_part, lse_part, split_indptr, num_partials, x.R, static_cast<uint16_t*>(out), lse);
+  return launch_status(cudaGetLastError());
 }
 
 mla_status mla_decode(const mla_desc* desc, const void* q, const void* kv_pages, const float* kv_scales,

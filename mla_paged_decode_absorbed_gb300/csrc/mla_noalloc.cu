@@ -6,8 +6,8 @@
 // forbid allocation afterwards (cudaMalloc may synchronise the device and
 // fragment a planned pool), and C callers that own only their input and output
 // buffers and have no allocator to draw a workspace from.  For them the
-// scratch this call needs (split plan, error word, fp32 partial outputs) lives
-// in a fixed array compiled into the library.
+// scratch this call needs (split plan, error word, the fp16 partial outputs of
+// split requests) lives in a fixed array compiled into the library.
 //
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes
 // (40 MiB).  Every GPU on which this module gets loaded holds it until the
@@ -69,5 +69,15 @@ extern "C" mla_status mla_decode_noalloc(const mla_desc* desc, const void* q, co
   mla_status st = mla_decode(&d, q, kv_pages, kv_scales, block_table, seqlens, s_q, softmax_scale, out, lse,
                              scratch, kNoAllocScratchBytes, stream);
   if (st != MLA_OK || !check_device_error) return st;
+  return mla_get_device_error(scratch, stream);
+}
+
+// The error word of the last mla_decode_noalloc() on the current device, for
+// callers that ran it without check_device_error (for instance from a
+// captured graph): synchronises `stream` and reads the word through the
+// scratch array's cached device address.
+extern "C" mla_status mla_noalloc_get_device_error(void* stream) {
+  void* scratch = scratch_address();
+  if (!scratch) return MLA_ERR_CUDA;
   return mla_get_device_error(scratch, stream);
 }

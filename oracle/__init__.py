@@ -57,12 +57,19 @@ def _load():
             lib.oracle_e4m3_to_f64.restype = ctypes.c_double
             lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.restype = None
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the next oracle calls use (a timing knob; results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def bf16_to_f64(code: int) -> float:

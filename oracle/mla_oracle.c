@@ -216,6 +216,16 @@ int oracle_mla_decode(const void* q, const void* kv, const float* kv_scales, int
   return status;
 }
 
+/* Thread count used by the next oracle_mla_decode calls (n >= 1); a timing
+ * knob only, the arithmetic is the same for any count. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 int oracle_num_threads(void) {
   int n = 1;
 #pragma omp parallel

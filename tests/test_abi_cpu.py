@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for need in ("mla_decode", "mla_plan", "mla_decode_attention", "mla_combine", "mla_workspace_size",
+    for need in ("mla_decode", "mla_plan", "mla_decode_attention", "mla_combine", "mla_combine_workspace",
+                 "mla_workspace_size",
                  "mla_get_device_error", "mla_status_string", "mla_num_clusters", "mla_get_workspace_layout"):
         assert need in names
 
@@ -117,6 +118,22 @@ def test_pointer_and_scalar_validation(lib):
         == mla.MLA_ERR_INVALID_ARG                             # fp8 needs scales
     for code in range(-8, 1):
         assert lib.mla_status_string(code).decode() != "unknown status"
+
+
+def test_combine_of_caller_partials_validates_before_any_launch(lib):
+    d = _desc()
+    ok = 1 << 20
+    call = lambda o, l, ip, n, out, lse: lib.mla_combine(ctypes.byref(d), o, l, ip, n, out, lse, None)
+    assert call(ok, ok, ok, -1, ok, ok) == mla.MLA_ERR_INVALID_ARG        # negative partial count
+    assert call(ok, ok, None, 4, ok, ok) == mla.MLA_ERR_INVALID_ARG       # no split_indptr
+    assert call(None, ok, ok, 4, ok, ok) == mla.MLA_ERR_INVALID_ARG       # partials without o_part
+    assert call(ok + 8, ok, ok, 4, ok, ok) == mla.MLA_ERR_INVALID_ARG     # o_part must be 16-byte aligned
+    assert call(ok, ok + 2, ok, 4, ok, ok) == mla.MLA_ERR_INVALID_ARG
+    assert call(ok, ok, ok, 4, ok + 8, ok) == mla.MLA_ERR_INVALID_ARG     # out must be 16-byte aligned
+    assert call(ok, ok, ok, 4, ok, None) == mla.MLA_ERR_INVALID_ARG
+    bad = _desc()
+    bad.page_size = 32
+    assert lib.mla_combine(ctypes.byref(bad), ok, ok, ok, 4, ok, ok, None) == mla.MLA_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------------ plan properties

@@ -83,6 +83,8 @@ def test_host_tensors_are_rejected_before_the_library_is_called():
     args = (t["q"], t["kv"], t["kv_scales"], t["block_table"], t["seqlens"], SQ, 0.07, t["out"], t["lse"])
     for call in (lambda: mla.mla_decode(d, *args, ws), lambda: mla.mla_decode_attention(d, *args, ws),
                  lambda: mla.mla_decode_noalloc(d, *args), lambda: mla.mla_plan(d, t["seqlens"], ws),
-                 lambda: mla.mla_combine(d, t["out"], t["lse"], ws)):
+                 lambda: mla.mla_combine_workspace(d, t["out"], t["lse"], ws),
+                 lambda: mla.mla_combine(d, torch.zeros((2, SQ * H, 512)), torch.zeros((2, SQ * H)),
+                                         torch.zeros((B + 1,), dtype=torch.int32), t["out"], t["lse"])):
         with pytest.raises(ValueError, match="CUDA tensor"):
             call()
