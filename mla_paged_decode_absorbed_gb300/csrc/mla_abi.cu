@@ -546,8 +546,9 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
                          const int32_t* bt, const int32_t* seqlens, float scale, void* out, float* lse,
                          cudaStream_t stream) {
   // page maps of the scorer and the accumulator: bf16, 9 and 8 swizzled
-  // 64-channel blocks; fp8, raw e4m3 chunks [0, kFp8ScorerBlocks) and
-  // [kFp8ScorerBlocks, 8), plus the RoPE chunk for the scorer
+  // 64-channel blocks; fp8, every raw e4m3 chunk of the row for the scorer
+  // (variant B: the 8 latent chunks, plus the two bf16 RoPE chunks by their
+  // own map) and the 8 latent chunks for the accumulator
   CUtensorMap map_s, map_a, map_r;
   std::memset(&map_r, 0, sizeof(map_r));
   {
@@ -555,12 +556,12 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
     if (p.x.fp8) {
       const int tb = p.x.rope_bf16 ? kFp8bRecord : kDqk;
       const int nch = p.x.rope_bf16 ? 8 : 9;
-      st = make_kv_map_fp8(kv, p.x.P, tb, nch, kFp8ScorerBlocks, &map_s);
-      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, tb, nch, 8 - kFp8ScorerBlocks, &map_a);
+      st = make_kv_map_fp8(kv, p.x.P, tb, nch, nch, &map_s);
+      if (st == MLA_OK) st = make_kv_map_fp8(kv, p.x.P, tb, nch, 8, &map_a);
       if (st == MLA_OK) {
         if (p.x.rope_bf16)  // the RoPE bf16 bytes [528, 656) of each record: 2 chunks
           st = make_kv_map_fp8(static_cast<const uint8_t*>(kv) + kFp8bRopeOffset, p.x.P, tb, 2, 2, &map_r);
-        else                // the RoPE e4m3 chunk (chunk 8 of the row)
+        else                // not read by variant A (its RoPE chunk is chunk 8 of map_s); a valid map all the same
           st = make_kv_map_fp8(kv, p.x.P, tb, nch, 1, &map_r);
       }
     } else {

@@ -56,20 +56,24 @@ constexpr int kBox = 64 * 64 * 2;                  // 64 tokens x 64 channels, 1
 constexpr int kStages = 3;
 constexpr int kStageS = 9 * kBox;                  // scorer: channels 0..575
 constexpr int kStageO = 8 * kBox;                  // accumulator: channels 0..511
-// fp8 cache: the scorer converts latent blocks [0, kSB) and the RoPE block,
-// the accumulator latent blocks [kSB, 8); each copies its latent blocks into
-// the other's ring stage.  A CTA's raw e4m3 chunks (64 tokens x 64 bytes each,
-// 64-byte swizzled) sit in the part of its stage that the other's copy fills.
-constexpr int kSB = kFp8ScorerBlocks;
+// fp8 cache: each CTA TMA-loads the raw e4m3 chunks of every block it needs
+// (64 tokens x 64 bytes each, 64-byte swizzled) into the top of its ring
+// stage and rewrites the stage in place as fp16: the scorer as the exact
+// codes (scales are applied to the scores in fp32), the accumulator as code x
+// scale (its V).  Raw chunk c of a stage sits at kRaw*Off + c * kRawSlot.
 constexpr int kRawSlot = 64 * 64;                  // one raw chunk: 64 tokens x 64 bytes
-constexpr int kRawOffS = kSB * kBox;               // scorer: raw chunks 0..kSB-1, then the RoPE chunk
-constexpr int kRawOffA = 0;                        // accumulator: raw chunks kSB..7
-constexpr int kRawBytesS = (kSB + 1) * kRawSlot;
-constexpr int kRawBytesSB = (kSB + 2) * kRawSlot;  // variant B: the RoPE is two chunks of bf16
-constexpr int kRawBytesA = (8 - kSB) * kRawSlot;
-static_assert(kRawOffS + kRawBytesSB <= 8 * kBox && kRawOffA + kRawBytesA <= kSB * kBox,
-              "raw chunks must lie in the region the peer's copy fills");
-static_assert(2 * (kSB + 1) <= 10 && 2 * (8 - kSB) <= 10, "at most 10 pieces per dequant thread");
+constexpr int kRawBytesS = 9 * kRawSlot;           // scorer, variant A: chunks 0..8
+constexpr int kRawBytesSB = 10 * kRawSlot;         // scorer, variant B: 8 latent chunks + 2 bf16 RoPE chunks
+constexpr int kRawBytesA = 8 * kRawSlot;           // accumulator: latent chunks 0..7
+constexpr int kRawOffS = 9 * kBox - kRawBytesS;    // top of the scorer's 72 KB stage
+constexpr int kRawOffSB = 9 * kBox - kRawBytesSB;
+constexpr int kRawOffA = 8 * kBox - kRawBytesA;    // top of the accumulator's 64 KB stage
+static_assert(kRawOffS % 1024 == 0 && kRawOffSB % 1024 == 0 && kRawOffA % 1024 == 0, "raw chunks 1024-aligned");
+// fp8 scorer: QK runs per scale group g (channels [128g, 128g+128), the RoPE
+// group 4 = [512, 576)) into a ring of kGroupSlots TMEM score buffers; the
+// softmax adds scale[token][g] * S_g in fp32.
+constexpr int kGroupSlots = 3;
+constexpr int kScaleSlotBytes = kGroups * 64 * 4;  // [group][token] fp32, one slot per ring stage
 constexpr int kPBytes = kRowsPerBlock * 64 * 2;    // P tile: 128 rows x 64 keys, SW128 K-major
 constexpr int kVecBytes = kRowsPerBlock * 4;       // one fp32 per row
 constexpr int kPartBytes = kPartChunks * kRowsPerBlock * 16;  // one fp16 partial slot (128 KB)
@@ -80,20 +84,27 @@ static_assert(kPartBytes <= kStages * kStageO, "a partial slot must fit in the p
 constexpr int kQStageBytes = 32 * 64;              // scorer: per softmax warp, 32 rows x 32 channels
 constexpr int kOffQStage = kStages * kStageS;      // scorer: Q transpose staging [4]
 constexpr int kScorerEnd = kOffQStage + 4 * kQStageBytes;
+// fp8 scorer: a smaller Q staging (32 rows x 16 channels per warp), then the
+// per-stage scale slots the softmax reads
+constexpr int kQStageBytesF8 = 32 * 32;
+constexpr int kOffScale = kOffQStage + 4 * kQStageBytesF8;
+constexpr int kScorerEndF8 = kOffScale + kStages * kScaleSlotBytes;
 constexpr int kOffP = kStages * kStageO;           // accumulator: P tiles [2]
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;     // accumulator: rescale factors [2][128]
 constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: (row sum, lse) [128]
 constexpr int kAccEnd = kOffL + kRowsPerBlock * 8;
 constexpr int kOffBars = kScorerEnd > kAccEnd ? kScorerEnd : kAccEnd;
+static_assert(kScorerEndF8 <= kOffBars, "fp8 scorer layout overlaps the barriers");
 constexpr int kBarBytes = 384;
 constexpr int kSmemMax = 232448;
 constexpr int kSmem = kSmemMax;                    // layout + slack for aligning the base
 constexpr int kAlignSlack = kSmem - kOffBars - kBarBytes;
 static_assert(kAlignSlack >= 0, "shared memory layout too large");
 
-// TMEM columns.  Scorer: Q (576 16-bit channels) then two S buffers.
-constexpr uint32_t kColQ = 0, kColS0 = 288, kColS1 = 352;
-
+// TMEM columns.  Scorer: Q (576 16-bit channels) then two S buffers (bf16
+// cache) or kGroupSlots per-group score buffers (fp8 cache).
+constexpr uint32_t kColQ = 0, kColS0 = 288, kColS1 = 352, kColG = 288;
+static_assert(kColG + 64 * kGroupSlots <= 512, "fp8 score slots exceed TMEM");
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -127,9 +138,9 @@ struct Bars {
                           // unlike bar.sync, so a warp that gives up cannot strand the others
   uint64_t drain;
   uint64_t raw_full[kStages];    // fp8: this CTA's raw e4m3 chunks arrived (1 + tx)
-  uint64_t dq_sync;              // fp8: the dequant threads wrote their blocks (128), bounded
-  uint64_t peer_empty[kStages];  // fp8: the peer's MMAs finished the stage (peer's multicast commit)
-  uint64_t raw_free[kStages];    // fp8: the peer read its raw chunks, our copy may land (remote, 1)
+  uint64_t dq_sync;              // fp8: the dequant threads read their raw chunks (128), bounded
+  uint64_t sg_full[kGroupSlots]; // fp8 scorer: QK of one scale group done (commit)
+  uint64_t sg_free[kGroupSlots]; // fp8 scorer: that group's scores read by the softmax (128)
   uint64_t stall;                // never signalled: the wait a test's stall request runs out on
   int abort_flag;
   uint32_t tmem_base;
@@ -275,6 +286,13 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint16_t v, __half2 hi, 
   return *reinterpret_cast<const uint32_t*>(&y);
 }
 
+// e4m3 x2 -> f16x2, exact (every e4m3 value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return h2;
+}
+
 // Tree reductions over 64 values (independent chains for ILP).
 __device__ __forceinline__ float max64(const float (&x)[64]) {
   float m[8];
@@ -309,9 +327,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // fp8: 128 dequant threads + the loader's expect_tx for the peer's copy
-      mbar_init(smem_u32(&bars->kv_full[s]), kFp8 ? 129 : 1);
-      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+      // fp8: the 128 dequant threads complete a stage; the fp8 scorer's stage
+      // is freed by its 128 softmax threads once they have read the stage's
+      // scales (the group commits they waited on imply its MMAs are done)
+      mbar_init(smem_u32(&bars->kv_full[s]), kFp8 ? 128 : 1);
+      mbar_init(smem_u32(&bars->kv_empty[s]), (kFp8 && scorer) ? 128 : 1);
     }
     mbar_init(smem_u32(&bars->q_full), 128);
     mbar_init(smem_u32(&bars->q_tma), 1);
@@ -332,10 +352,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(smem_u32(&bars->mrg_bar), 1);
     mbar_init(smem_u32(&bars->epi_bar), 128);
     mbar_init(smem_u32(&bars->drain), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->raw_full[s]), 1);
-      mbar_init(smem_u32(&bars->peer_empty[s]), 1);
-      mbar_init(smem_u32(&bars->raw_free[s]), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars->raw_full[s]), 1);
+    for (int s = 0; s < kGroupSlots; ++s) {
+      mbar_init(smem_u32(&bars->sg_full[s]), 1);
+      mbar_init(smem_u32(&bars->sg_free[s]), 128);
     }
     mbar_init(smem_u32(&bars->stall), 1);
     mbar_init(smem_u32(&bars->dq_sync), 128);
@@ -443,17 +463,17 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               const uint32_t fb = smem_u32(kFp8 ? &bars->raw_full[stage] : &bars->kv_full[stage]);
               uint8_t* dst = smem + stage * stage_bytes;
               if (kFp8) {
-                // the peer's converted blocks will complete on kv_full
-                mbar_arrive_expect_tx(smem_u32(&bars->kv_full[stage]),
-                                      static_cast<uint32_t>(scorer ? (8 - kSB) * kBox : kSB * kBox));
+                // every raw chunk this CTA converts, into the top of its stage
                 mbar_arrive_expect_tx(
                     fb, static_cast<uint32_t>(scorer ? (kRopeB ? kRawBytesSB : kRawBytesS) : kRawBytesA));
                 if (scorer) {
-                  tma_load_4d(smem_u32(dst + kRawOffS), &kv_map_s, 0, 0, 0, pid, fb);
-                  // the RoPE: chunk 8 of an e4m3 row, or the two bf16 chunks of a variant B record
-                  tma_load_4d(smem_u32(dst + kRawOffS + kSB * kRawSlot), &kv_map_r, 0, 0, kRopeB ? 0 : 8, pid, fb);
+                  const int off = kRopeB ? kRawOffSB : kRawOffS;
+                  // variant A: chunks 0..8 of the e4m3 row; variant B: the 8 latent chunks
+                  tma_load_4d(smem_u32(dst + off), &kv_map_s, 0, 0, 0, pid, fb);
+                  // variant B: the two bf16 RoPE chunks of the record
+                  if (kRopeB) tma_load_4d(smem_u32(dst + off + 8 * kRawSlot), &kv_map_r, 0, 0, 0, pid, fb);
                 } else {
-                  tma_load_4d(smem_u32(dst + kRawOffA), &kv_map_a, 0, 0, kSB, pid, fb);
+                  tma_load_4d(smem_u32(dst + kRawOffA), &kv_map_a, 0, 0, 0, pid, fb);
                 }
               } else if (scorer) {
                 mbar_arrive_expect_tx(fb, bytes);
@@ -505,7 +525,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     if (scorer) {
       // S[b] = Q K^T: 36 steps of K=16 over the 576 channels, A = Q in TMEM.
+      // fp8 cache: the same steps over the exact e4m3 codes, one MMA chain per
+      // scale group (8 steps per latent group of 128 channels, 4 for the RoPE)
+      // into the next slot of the group-score ring; the softmax applies the
+      // tokens' scales and frees the stage.
       const uint32_t idesc = idesc_f16_f32(128, 64, false, false, !kFp8);
+      uint32_t gj = 0;  // fp8: group-score ring counter over the whole kernel
       while (ok && it.next(s)) {
         if (s.empty) continue;
         if (!mbar_wait(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
@@ -513,20 +538,41 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
           if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&bars->s_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t b0 = smem_desc_sw128(smem_u32(smem + stage * kStageS), 16, 1024);
-            const uint32_t dcol = tbase + (sb ? kColS1 : kColS0);
+          const uint64_t b0 = smem_desc_sw128(smem_u32(smem + stage * kStageS), 16, 1024);
+          if (kFp8) {
+            for (int g = 0; g < kGroups && ok; ++g, ++gj) {
+              const uint32_t slot = gj % kGroupSlots, gph = (gj / kGroupSlots) & 1u;
+              // warp-uniform outcome: the issue below ends in __syncwarp
+              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_free[slot]), gph ^ 1u, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (lane == 0) {
+                const uint32_t dcol = tbase + kColG + 64 * slot;
+                const int k0 = 8 * g, k1 = g < 4 ? 8 * g + 8 : 36;
+                for (int k = k0; k < k1; ++k)
+                  mma_ts(dcol, tbase + kColQ + 8 * k, b0 + static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4),
+                         idesc, k > k0 ? 1u : 0u);
+                mma_commit(smem_u32(&bars->sg_full[slot]));
+              }
+              __syncwarp();
+            }
+            if (!ok) break;
+          } else {
+            if (!mbar_wait(smem_u32(&bars->s_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t dcol = tbase + (sb ? kColS1 : kColS0);
 #pragma unroll
-            for (int k = 0; k < 36; ++k)
-              mma_ts(dcol, tbase + kColQ + 8 * k, b0 + static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4),
-                     idesc, k > 0 ? 1u : 0u);
-            mma_commit(smem_u32(&bars->s_full[sb]));
-            mma_commit(smem_u32(&bars->kv_empty[stage]));
-            if (kFp8) mma_commit_multicast(smem_u32(&bars->peer_empty[stage]), static_cast<uint16_t>(1u << peer));
+              for (int k = 0; k < 36; ++k)
+                mma_ts(dcol, tbase + kColQ + 8 * k, b0 + static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4),
+                       idesc, k > 0 ? 1u : 0u);
+              mma_commit(smem_u32(&bars->s_full[sb]));
+              mma_commit(smem_u32(&bars->kv_empty[stage]));
+            }
+            __syncwarp();
           }
-          __syncwarp();
           if (++stage == kStages) {
             stage = 0;
             ph ^= 1u;
@@ -565,7 +611,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                        vb + static_cast<uint64_t>((h * 4 * kBox + k * 2048) >> 4), idesc,
                        (j > s.page_lo || k > 0) ? 1u : 0u);
             mma_commit(smem_u32(&bars->kv_empty[stage]));
-            if (kFp8) mma_commit_multicast(smem_u32(&bars->peer_empty[stage]), static_cast<uint16_t>(1u << peer));
             mma_commit(smem_u32(&bars->pv_done[sb]));
             // P buffer sb may be refilled by the scorer once this PV is done; the
             // buffer of a segment's last tile is returned by the epilogue instead,
@@ -606,16 +651,15 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const uint32_t rLfull = mapa_shared(smem_u32(&bars->l_full), peer);
       uint32_t q_loaded = 0;
       float qmul = 1.f, qmul_next = 1.f;
+      uint32_t gj = 0;  // fp8: group-score ring counter (advances like the MMA warp's)
 
       // Q rows of this warp (its TMEM lane quarter) -> TMEM, all 576 channels
       // (the A operand of QK).  The loads are coalesced: per 32-channel step
       // a warp instruction reads 8 rows x 64 contiguous bytes, and the step
       // is transposed through a 2 KB shared staging area so that each thread
-      // then holds its own row for tcgen05.st.  The fp8-cache variant computes
-      // in fp16: the row is scaled by a power of two so |q| <= 16384 (no
-      // overflow), undone on the scores.
+      // then holds its own row for tcgen05.st.
       uint8_t* const qst = smem + kOffQStage + wq * kQStageBytes;
-      auto load_q = [&](const Seg& sg) -> float {
+      auto load_q_bf16 = [&](const Seg& sg) {
         const int r0 = sg.rb * kRowsPerBlock + wq * 32;  // first row of this warp
         const int rsub = lane >> 2, csub = lane & 3;     // load view: rows rsub + 8i, 16-byte chunk csub
         const uint8_t* qb = reinterpret_cast<const uint8_t*>(a.q) + static_cast<size_t>(sg.b) * a.R * (kDqk * 2);
@@ -626,43 +670,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           const int r = r0 + rsub + 8 * i;
           rv[i] = r < a.R;
           rp[i] = qb + static_cast<size_t>(rv[i] ? r : 0) * (kDqk * 2) + csub * 16;
-        }
-        float qs = 1.f, qm = 1.f;
-        if (kFp8) {
-          float am[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int s0 = 0; s0 < 18; s0 += 6) {
-            uint4 x[24];
-#pragma unroll
-            for (int st = 0; st < 6; ++st)
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                x[4 * st + i] = rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (s0 + st) * 64))
-                                      : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int v = 0; v < 24; ++v) {
-              const uint4 y = x[v];
-              const float m = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(y.x)), fabsf(bf16_hi(y.x))),
-                                          fmaxf(fabsf(bf16_lo(y.y)), fabsf(bf16_hi(y.y)))),
-                                    fmaxf(fmaxf(fabsf(bf16_lo(y.z)), fabsf(bf16_hi(y.z))),
-                                          fmaxf(fabsf(bf16_lo(y.w)), fabsf(bf16_hi(y.w)))));
-              am[v & 3] = fmaxf(am[v & 3], m);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], 1));
-            am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], 2));
-          }
-          // row `lane` of the warp was read by lanes 4 * (lane & 7) + 0..3, as its (lane >> 3)-th row
-          const int src = 4 * (lane & 7);
-          const float v0 = __shfl_sync(0xffffffffu, am[0], src), v1 = __shfl_sync(0xffffffffu, am[1], src);
-          const float v2 = __shfl_sync(0xffffffffu, am[2], src), v3 = __shfl_sync(0xffffffffu, am[3], src);
-          const int sel = lane >> 3;
-          const float amax = sel == 0 ? v0 : (sel == 1 ? v1 : (sel == 2 ? v2 : v3));
-          int k = 0;
-          while (k < 126 && amax * ldexpf(1.f, -k) > 16384.f) ++k;
-          qs = ldexpf(1.f, -k);
-          qm = ldexpf(1.f, k);
         }
         for (int s0 = 0; s0 < 18; s0 += 6) {
           uint4 x[24];
@@ -684,13 +691,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-              uint4 y = *reinterpret_cast<const uint4*>(qst + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4));
-              if (kFp8) {
-                y.x = pack_f16x2(bf16_lo(y.x) * qs, bf16_hi(y.x) * qs);
-                y.y = pack_f16x2(bf16_lo(y.y) * qs, bf16_hi(y.y) * qs);
-                y.z = pack_f16x2(bf16_lo(y.z) * qs, bf16_hi(y.z) * qs);
-                y.w = pack_f16x2(bf16_lo(y.w) * qs, bf16_hi(y.w) * qs);
-              }
+              const uint4 y = *reinterpret_cast<const uint4*>(qst + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4));
               w[4 * c4 + 0] = y.x;
               w[4 * c4 + 1] = y.y;
               w[4 * c4 + 2] = y.z;
@@ -703,7 +704,89 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->q_full));
-        return qm;
+      };
+      // fp8 cache: the MMAs run in fp16, so each row is first scaled by a power
+      // of two that puts |q| <= 16384 (no overflow; undone on the scores).
+      // Same coalesced scheme with 16-channel half-steps through a 1 KB
+      // staging area per warp (the rest of the space holds the scale slots).
+      uint8_t* const qst8 = smem + kOffQStage + wq * kQStageBytesF8;
+      auto load_q_f16 = [&](const Seg& sg) -> float {
+        const int r0 = sg.rb * kRowsPerBlock + wq * 32;
+        const int rsub = lane >> 1, csub = lane & 1;     // load view: rows rsub + 16i, 16-byte chunk csub of 32
+        const uint8_t* qb = reinterpret_cast<const uint8_t*>(a.q) + static_cast<size_t>(sg.b) * a.R * (kDqk * 2);
+        bool rv[2];
+        const uint8_t* rp[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = r0 + rsub + 16 * i;
+          rv[i] = r < a.R;
+          rp[i] = qb + static_cast<size_t>(rv[i] ? r : 0) * (kDqk * 2) + csub * 16;
+        }
+        float am[2] = {0.f, 0.f};
+        for (int h0 = 0; h0 < 36; h0 += 12) {
+          uint4 x[24];
+#pragma unroll
+          for (int u = 0; u < 12; ++u)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              x[2 * u + i] = rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (h0 + u) * 32)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int v = 0; v < 24; ++v) {
+            const uint4 y = x[v];
+            const float m = fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(y.x)), fabsf(bf16_hi(y.x))),
+                                        fmaxf(fabsf(bf16_lo(y.y)), fabsf(bf16_hi(y.y)))),
+                                  fmaxf(fmaxf(fabsf(bf16_lo(y.z)), fabsf(bf16_hi(y.z))),
+                                        fmaxf(fabsf(bf16_lo(y.w)), fabsf(bf16_hi(y.w)))));
+            am[v & 1] = fmaxf(am[v & 1], m);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], 1));
+        // row `lane` of the warp was read by lanes 2 * (lane & 15) + 0..1, as its (lane >> 4)-th row
+        const float v0 = __shfl_sync(0xffffffffu, am[0], 2 * (lane & 15));
+        const float v1 = __shfl_sync(0xffffffffu, am[1], 2 * (lane & 15));
+        const float amax = (lane >> 4) ? v1 : v0;
+        int k = 0;
+        while (k < 126 && amax * ldexpf(1.f, -k) > 16384.f) ++k;
+        const float qs = ldexpf(1.f, -k);
+        for (int h0 = 0; h0 < 36; h0 += 12) {
+          uint4 x[24];
+#pragma unroll
+          for (int u = 0; u < 12; ++u)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              x[2 * u + i] = rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (h0 + u) * 32)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 12; ++u) {
+            // staging row rr at rr * 32, its 16-byte chunk c at (c ^ ((rr >> 2) & 1)) (no bank conflicts)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int rr = rsub + 16 * i;
+              *reinterpret_cast<uint4*>(qst8 + rr * 32 + ((csub ^ ((rr >> 2) & 1)) << 4)) = x[2 * u + i];
+            }
+            __syncwarp();
+            uint32_t w[8];
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const uint4 y = *reinterpret_cast<const uint4*>(qst8 + lane * 32 + ((c2 ^ ((lane >> 2) & 1)) << 4));
+              w[4 * c2 + 0] = pack_f16x2(bf16_lo(y.x) * qs, bf16_hi(y.x) * qs);
+              w[4 * c2 + 1] = pack_f16x2(bf16_lo(y.y) * qs, bf16_hi(y.y) * qs);
+              w[4 * c2 + 2] = pack_f16x2(bf16_lo(y.z) * qs, bf16_hi(y.z) * qs);
+              w[4 * c2 + 3] = pack_f16x2(bf16_lo(y.w) * qs, bf16_hi(y.w) * qs);
+            }
+            __syncwarp();
+            tmem_st8(tbase + lane_off + kColQ + 8 * (h0 + u), w);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->q_full));
+        return ldexpf(1.f, k);
+      };
+      auto load_q = [&](const Seg& sg) -> float {
+        if (kFp8) return load_q_f16(sg);
+        load_q_bf16(sg);
+        return 1.f;
       };
       // bf16, first segment: the Q block was brought into ring stages 1-2 by
       // TMA (row r, chunk c at line 9r + c of the 128-byte-swizzled box); each
@@ -774,10 +857,58 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 break;
               }
           }
-          if (!mbar_wait(smem_u32(&bars->s_full[sb]), sph, abort_flag)) { ok = false; break; }
-          tc_fence_after();
           float x[64];
-          {
+          if (kFp8) {
+            // S = sum_g scale[token][g] * S_g, in fp32 from the group-score ring;
+            // the tokens' scales are in the scale slot of the tile's stage
+            const int stg = static_cast<int>(t % kStages);
+            const float* scl = reinterpret_cast<const float*>(smem + kOffScale + stg * kScaleSlotBytes);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = 0.f;
+            for (int g = 0; g < kGroups; ++g, ++gj) {
+              const uint32_t slot = gj % kGroupSlots, gph = (gj / kGroupSlots) & 1u;
+              // warp-uniform outcome: tcgen05.ld below is a warp-wide instruction
+              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), gph, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              uint32_t v0[32], v1[32];
+              const uint32_t col = tbase + lane_off + kColG + 64 * slot;
+              tmem_ld32(col, v0);
+              tmem_ld32(col + 32, v1);
+              tmem_wait_ld();
+              tc_fence_before();
+              mbar_arrive(smem_u32(&bars->sg_free[slot]));
+              // the dequant threads wrote the scales before completing the stage
+              if (g == 0 &&
+                  !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[stg]), (t / kStages) & 1u, abort_flag))) {
+                ok = false;
+                break;
+              }
+              const float4* sc4 = reinterpret_cast<const float4*>(scl + g * 64);
+#pragma unroll
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 a = sc4[i4], b = sc4[8 + i4];
+                x[4 * i4 + 0] = fmaf(__uint_as_float(v0[4 * i4 + 0]), a.x, x[4 * i4 + 0]);
+                x[4 * i4 + 1] = fmaf(__uint_as_float(v0[4 * i4 + 1]), a.y, x[4 * i4 + 1]);
+                x[4 * i4 + 2] = fmaf(__uint_as_float(v0[4 * i4 + 2]), a.z, x[4 * i4 + 2]);
+                x[4 * i4 + 3] = fmaf(__uint_as_float(v0[4 * i4 + 3]), a.w, x[4 * i4 + 3]);
+                x[32 + 4 * i4 + 0] = fmaf(__uint_as_float(v1[4 * i4 + 0]), b.x, x[32 + 4 * i4 + 0]);
+                x[32 + 4 * i4 + 1] = fmaf(__uint_as_float(v1[4 * i4 + 1]), b.y, x[32 + 4 * i4 + 1]);
+                x[32 + 4 * i4 + 2] = fmaf(__uint_as_float(v1[4 * i4 + 2]), b.z, x[32 + 4 * i4 + 2]);
+                x[32 + 4 * i4 + 3] = fmaf(__uint_as_float(v1[4 * i4 + 3]), b.w, x[32 + 4 * i4 + 3]);
+              }
+            }
+            if (!ok) break;
+            // scales read and every QK MMA of the page done: the stage may be refilled
+            mbar_arrive(smem_u32(&bars->kv_empty[stg]));
+            const int nv = n_vis - j * kPage;  // keys of this page visible to the row
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = i < nv ? x[i] * row_scale : -INFINITY;
+          } else {
+            if (!mbar_wait(smem_u32(&bars->s_full[sb]), sph, abort_flag)) { ok = false; break; }
+            tc_fence_after();
             uint32_t v0[32], v1[32];
             const uint32_t col = tbase + lane_off + (sb ? kColS1 : kColS0);
             tmem_ld32(col, v0);
@@ -1155,36 +1286,28 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     if (!scorer && lane == 0) bulk_wait_all();  // output stores complete before the CTA ends
   } else if (kFp8) {
     // ---------------------------------------------------------------- fp8 dequant (warps 6-9)
-    // This CTA's raw chunks (64-byte swizzled) -> e4m3 x scale as fp16 in its
-    // own latent blocks (scorer: [0, kSB) and the RoPE block; accumulator:
-    // [kSB, 8)), 128-byte swizzled as the MMA descriptors expect.  Thread =
-    // (token t = lane-major, half h); each converts n 16-channel pieces.  Then
-    // one thread copies the latent blocks into the peer's stage once the peer
-    // has read its raw chunks there.  Rows past seqlen (and pages with a bad
-    // id, which TMA reads as zeros) are written as zeros.
+    // This CTA's raw e4m3 chunks (64-byte swizzled, in the top of its stage)
+    // -> fp16 blocks of the same stage, 128-byte swizzled as the MMA
+    // descriptors expect.  The scorer writes the exact codes of its 9 blocks
+    // (variant B: the 8 latent blocks, and the RoPE block from bf16) and the
+    // tokens' group scales into the stage's scale slot; the accumulator writes
+    // code x scale for the 8 latent blocks.  Thread = (token t, half h): it
+    // reads all its raw pieces into registers, the 128 threads meet (the fp16
+    // blocks overwrite the raw chunks in place), then it converts and writes.
+    // Rows past seqlen and pages with a bad id (read as zeros by TMA) are
+    // written as zeros, with scale 0.
     const int dq = tid - 192;                       // 0..127
     const int t = dq & 63, h = dq >> 6;
-    const int n = scorer ? 2 * (kSB + 1) : 2 * (8 - kSB);  // 16-channel pieces per thread
-    // piece f of a token: raw slot f >> 2, quarter f & 3; its channel
-    auto piece_ch = [&](int f) -> int {
-      const int slot = f >> 2;
-      const int chunk = scorer ? (slot < kSB ? slot : 8) : kSB + slot;
-      return 64 * chunk + 16 * (f & 3);
-    };
-    auto group_of = [](int c) -> int { return c < 512 ? (c >> 7) : 4; };
-    const int g_lo = group_of(piece_ch(n * h)), g_hi = group_of(piece_ch(n * h + n - 1));
-    const uint32_t raw_off = static_cast<uint32_t>(scorer ? kRawOffS : kRawOffA);
-    // latent blocks this CTA sends, at the same offsets in the peer's stage
-    const uint32_t send_off = static_cast<uint32_t>(scorer ? 0 : kSB * kBox);
-    const uint32_t send_bytes = static_cast<uint32_t>(scorer ? kSB * kBox : (8 - kSB) * kBox);
-    const int peer_stage_bytes = scorer ? kStageO : kStageS;
-    const uint32_t peer_smem = mapa_shared(smem_u32(smem), peer);
+    constexpr int kPieces = 18;                     // 16-channel pieces per thread (the scorer's count)
+    const int n = scorer ? 18 : 16;                 // scorer: 36 pieces per token; accumulator: 32
+    const int f0 = n * h;
+    const uint32_t raw_off = static_cast<uint32_t>(scorer ? (kRopeB ? kRawOffSB : kRawOffS) : kRawOffA);
     const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(a.kv);
     SegIter it = it0;
     Seg s;
     int stage = 0;
     uint32_t ph = 0, sync_ph = 0;
-    bool ok = true, sent_any = false;
+    bool ok = true;
     while (ok && it.next(s)) {
       if (s.empty) continue;
       const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
@@ -1197,102 +1320,128 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         const int pid = __shfl_sync(0xffffffffu, ids, slot);
         const bool bad = pid < 0 || pid >= a.num_pages;  // the loader reports it
         const bool live = !bad && t < seqlen - p * kPage;
-        float s_lo = 0.f, s_hi = 0.f;
-        if (live) {
-          const size_t row = static_cast<size_t>(pid) * kPage + t;
-          if (kRopeB) {  // four latent scales in the record (the RoPE has none)
-            const float* sp = reinterpret_cast<const float*>(kv8 + row * kFp8bRecord + kFp8bScaleOffset);
-            s_lo = __ldg(sp + min(g_lo, 3));
-            s_hi = __ldg(sp + min(g_hi, 3));
+        const size_t row = static_cast<size_t>(live ? pid : 0) * kPage + t;
+        // scales of this thread's groups: the accumulator's two latent groups
+        // (2h, 2h + 1); the scorer's half-0 threads fetch all five for the softmax
+        float sg[kGroups] = {0.f, 0.f, 0.f, 0.f, 0.f};
+        if (live && (!scorer || h == 0)) {
+          if (kRopeB) {
+            const float4 s4 = __ldg(reinterpret_cast<const float4*>(kv8 + row * kFp8bRecord + kFp8bScaleOffset));
+            sg[0] = s4.x;
+            sg[1] = s4.y;
+            sg[2] = s4.z;
+            sg[3] = s4.w;
+            sg[4] = 1.f;  // the bf16 RoPE carries no scale
           } else {
             const float* sp = a.kv_scales + row * kGroups;
-            s_lo = __ldg(sp + g_lo);
-            s_hi = __ldg(sp + g_hi);
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) sg[g] = __ldg(sp + g);
           }
         }
-        // our blocks of this stage were copied to the peer three pages ago:
-        // reuse them only after the peer's MMAs are done with that page
-        if (!mbar_wait<true>(smem_u32(&bars->peer_empty[stage]), ph ^ 1u, abort_flag)) {
+        // warp-uniform outcomes (the page-id shuffle above is warp-wide)
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->raw_full[stage]), ph, abort_flag))) {
           ok = false;
           break;
         }
-        if (!mbar_wait(smem_u32(&bars->raw_full[stage]), ph, abort_flag)) {
-          ok = false;
-          break;
-        }
-        bool out_of_range = live && !(fmaxf(fabsf(s_lo), fabsf(s_hi)) * 448.f <= 65504.f);
-        const __half hl = __float2half_rn(s_lo), hh = __float2half_rn(s_hi);
-        const __half ll = __float2half_rn(s_lo - __half2float(hl)), lh = __float2half_rn(s_hi - __half2float(hh));
-        uint8_t* const dst = smem + stage * stage_bytes;
+        uint8_t* const dst = smem + stage * (scorer ? kStageS : kStageO);
         const uint8_t* const raw = dst + raw_off + t * 64;
         const int sw = t & 7, rsw = (t >> 1) & 3;
+        // raw pieces -> registers (variant B RoPE pieces, f >= 32, are 32 bytes of bf16)
+        uint4 ra[kPieces], rb[4];
 #pragma unroll
-        for (int i = 0; i < 10; ++i) {
-          if (i < n) {
-            const int f = n * h + i;
-            const int c = piece_ch(f);
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (kRopeB && live && c >= kDv) {
-              // variant B RoPE piece: 16 bf16 channels (two 16-byte granules of
-              // the two RoPE chunks) -> fp16, exact inside the fp16 range
-              const int qr = f & 3;
-              const uint8_t* rr = raw + (kSB + (qr >> 1)) * kRawSlot;
-              const uint4 r0 = *reinterpret_cast<const uint4*>(rr + (((2 * (qr & 1)) ^ rsw) << 4));
-              const uint4 r1 = *reinterpret_cast<const uint4*>(rr + (((2 * (qr & 1) + 1) ^ rsw) << 4));
-              const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-              uint32_t hw[8];
-              float amax = 0.f;
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
-                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
-                hw[k] = pack_f16x2(lo, hi);
-              }
-              out_of_range |= !(amax <= 65504.f);
-              o0 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              o1 = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-            } else if (live) {
-              const uint4 r = *reinterpret_cast<const uint4*>(raw + (f >> 2) * kRawSlot + (((f & 3) ^ rsw) << 4));
-              const bool lo = group_of(c) == g_lo;
-              const __half2 shi = __half2half2(lo ? hl : hh), slo = __half2half2(lo ? ll : lh);
-              o0.x = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.x & 0xFFFFu), shi, slo);
-              o0.y = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.x >> 16), shi, slo);
-              o0.z = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.y & 0xFFFFu), shi, slo);
-              o0.w = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.y >> 16), shi, slo);
-              o1.x = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.z & 0xFFFFu), shi, slo);
-              o1.y = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.z >> 16), shi, slo);
-              o1.z = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.w & 0xFFFFu), shi, slo);
-              o1.w = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.w >> 16), shi, slo);
+        for (int i = 0; i < kPieces; ++i) {
+          ra[i] = make_uint4(0, 0, 0, 0);
+          const int f = f0 + i;
+          if (i < n && live) {
+            if (kRopeB && f >= 32) {
+              const int qr = f - 32;
+              const uint8_t* rr = raw + (8 + (qr >> 1)) * kRawSlot;
+              ra[i] = *reinterpret_cast<const uint4*>(rr + (((2 * (qr & 1)) ^ rsw) << 4));
+              if (i >= kPieces - 4) rb[i - (kPieces - 4)] = *reinterpret_cast<const uint4*>(rr + (((2 * (qr & 1) + 1) ^ rsw) << 4));
+            } else {
+              ra[i] = *reinterpret_cast<const uint4*>(raw + (f >> 2) * kRawSlot + (((f & 3) ^ rsw) << 4));
             }
-            const int c8 = (c & 63) >> 3;
-            uint8_t* const row = dst + (c >> 6) * kBox + t * 128;
-            *reinterpret_cast<uint4*>(row + ((c8 ^ sw) << 4)) = o0;
-            *reinterpret_cast<uint4*>(row + (((c8 + 1) ^ sw) << 4)) = o1;
           }
         }
-        if (out_of_range) atomicOr(a.err, kErrRange);
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&bars->kv_full[stage]));
+        // every thread has its raw pieces: the fp16 blocks may now overwrite them
         mbar_arrive(smem_u32(&bars->dq_sync));
-        if (!mbar_wait(smem_u32(&bars->dq_sync), sync_ph, abort_flag)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dq_sync), sync_ph, abort_flag))) {
           ok = false;
           break;
         }
         sync_ph ^= 1u;
-        if (dq == 0) {
-          // our raw chunks are read: the peer's copy may land on them
-          mbar_arrive_remote(mapa_shared(smem_u32(&bars->raw_free[stage]), peer));
-          if (!mbar_wait<true>(smem_u32(&bars->raw_free[stage]), ph, abort_flag)) {
-            ok = false;
-          } else {
-            const uint32_t poff = static_cast<uint32_t>(stage * peer_stage_bytes) + send_off;
-            bulk_copy_peer(peer_smem + poff, smem_u32(dst + send_off), send_bytes,
-                           mapa_shared(smem_u32(&bars->kv_full[stage]), peer));
-            sent_any = true;
+        bool out_of_range = false;
+        __half2 shi[2], slo[2];
+        if (!scorer) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const float sv = sg[2 * h + q];
+            out_of_range |= live && !(fabsf(sv) * 448.f <= 65504.f);
+            const __half hs = __float2half_rn(sv);
+            shi[q] = __half2half2(hs);
+            slo[q] = __half2half2(__float2half_rn(sv - __half2float(hs)));
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+#pragma unroll
+        for (int i = 0; i < kPieces; ++i) {
+          if (i < n) {
+            const int f = f0 + i;
+            const int c = 64 * (f >> 2) + 16 * (f & 3);  // first channel of the piece (variant B RoPE: 512 + 16 qr)
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (live) {
+              const uint4 r = ra[i];
+              if (kRopeB && f >= 32) {
+                // 16 bf16 RoPE channels -> fp16, exact inside the fp16 range
+                const uint4 r1 = i >= kPieces - 4 ? rb[i - (kPieces - 4)] : make_uint4(0, 0, 0, 0);
+                const uint32_t w[8] = {r.x, r.y, r.z, r.w, r1.x, r1.y, r1.z, r1.w};
+                uint32_t hw[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
+                  amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                  hw[k] = pack_f16x2(lo, hi);
+                }
+                out_of_range |= !(amax <= 65504.f);
+                o0 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                o1 = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+              } else if (scorer) {
+                // the exact codes (every e4m3 value is an fp16 value)
+                o0.x = e4m3x2_f16x2(static_cast<uint16_t>(r.x & 0xFFFFu));
+                o0.y = e4m3x2_f16x2(static_cast<uint16_t>(r.x >> 16));
+                o0.z = e4m3x2_f16x2(static_cast<uint16_t>(r.y & 0xFFFFu));
+                o0.w = e4m3x2_f16x2(static_cast<uint16_t>(r.y >> 16));
+                o1.x = e4m3x2_f16x2(static_cast<uint16_t>(r.z & 0xFFFFu));
+                o1.y = e4m3x2_f16x2(static_cast<uint16_t>(r.z >> 16));
+                o1.z = e4m3x2_f16x2(static_cast<uint16_t>(r.w & 0xFFFFu));
+                o1.w = e4m3x2_f16x2(static_cast<uint16_t>(r.w >> 16));
+              } else {
+                const int q = (c >> 7) - 2 * h;           // which of the thread's two groups
+                const __half2 hh = q ? shi[1] : shi[0], ll = q ? slo[1] : slo[0];
+                o0.x = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.x & 0xFFFFu), hh, ll);
+                o0.y = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.x >> 16), hh, ll);
+                o0.z = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.y & 0xFFFFu), hh, ll);
+                o0.w = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.y >> 16), hh, ll);
+                o1.x = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.z & 0xFFFFu), hh, ll);
+                o1.y = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.z >> 16), hh, ll);
+                o1.z = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.w & 0xFFFFu), hh, ll);
+                o1.w = e4m3x2_scaled_f16x2(static_cast<uint16_t>(r.w >> 16), hh, ll);
+              }
+            }
+            const int c8 = (c & 63) >> 3;
+            uint8_t* const rowp = dst + (c >> 6) * kBox + t * 128;
+            *reinterpret_cast<uint4*>(rowp + ((c8 ^ sw) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowp + (((c8 + 1) ^ sw) << 4)) = o1;
+          }
+        }
+        if (scorer && h == 0) {  // the tokens' scales for the softmax, [group][token]
+          float* slot_sc = reinterpret_cast<float*>(smem + kOffScale + stage * kScaleSlotBytes);
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) slot_sc[g * 64 + t] = sg[g];
+        }
+        if (out_of_range) atomicOr(a.err, kErrRange);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bars->kv_full[stage]));
         if (++stage == kStages) {
           stage = 0;
           ph ^= 1u;
@@ -1300,10 +1449,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       }
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
-    // After an abort the peer may leave soon: give a copy just issued to it
-    // time to land (copies take microseconds) before this CTA reaches the end.
-    if (!ok && sent_any)
-      for (int i = 0; i < 100; ++i) __nanosleep(1000);
   }
 
   __syncwarp();

@@ -12,7 +12,6 @@ constexpr int kDqk = 576;            // channels per query head / KV token (512 
 constexpr int kDv = 512;             // output channels (latent part of a KV row)
 constexpr int kRowsPerBlock = 128;   // query rows (token-major (i, h)) per work unit = MMA M
 constexpr int kGroups = 5;           // fp8 scale groups per token
-constexpr int kFp8ScorerBlocks = 3;  // fp8: latent 64-channel blocks the scorer converts (rest: accumulator)
 constexpr int kFp8bRecord = 656;     // fp8 variant B bytes per token: e4m3 latent, 4 fp32 scales, RoPE bf16
 constexpr int kFp8bScaleOffset = 512, kFp8bRopeOffset = 528;
 constexpr int kDefaultOverhead = 2;  // planner cost per work unit, in pages
@@ -78,9 +77,10 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters);
 // pages) with a chunk stride of 128 bytes; one box brings chunks 0..8 (scorer)
 // or 0..7 (accumulator) of a page as consecutive 64-token x 64-channel
 // swizzled blocks.  fp8 cache: the e4m3 bytes as a 4-D tensor (64 bytes, 64
-// tokens, 9 chunks, pages), 64-byte swizzled; boxes of kFp8ScorerBlocks
-// (scorer) or 8 - kFp8ScorerBlocks (accumulator) chunks, and kv_map_r one
-// chunk (the scorer's RoPE chunk).  kv_map_r is unused for the bf16 cache.
+// tokens, 9 chunks (variant B: 8 latent chunks of a 656-byte record),
+// pages), 64-byte swizzled; boxes of every chunk (scorer) or the 8 latent
+// chunks (accumulator), and kv_map_r the two bf16 RoPE chunks of a variant B
+// record.  kv_map_r is unused for the bf16 cache and fp8 variant A.
 // q_map: q as a 4-D tensor (64 channels, 9 channel chunks, R rows, B) whose
 // box (64, 9, 64, 1) is half a row block (rows past R read as zeros).
 // out_map: out as a 3-D tensor (512 channels, R rows, B) whose box

@@ -35,41 +35,9 @@ def run_gpu(inp, max_clusters: int = 0, plan_overhead: int = 0, decoder=None, te
     return o, l, status, dec
 
 
-def fp16_k_lse_shift(inp, rows=None):
-    """Per row, how far the oracle's lse moves when the dequantised fp8 cache
-    (e4m3 x scale) is rounded to fp16 before use -- the rounding the fp8
-    variant's 16-bit tensor-core operands cannot avoid.  Computed on the CPU
-    by running the oracle twice on fp64 caches built here with torch (the
-    exact product and its fp16 rounding); nothing comes from the CUDA path."""
-    import oracle
-    if getattr(inp, "rope_bf16", False):  # variant B records
-        rec = inp.kv
-        lat = rec[:, :, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
-        sc4 = rec[:, :, 512:528].contiguous().view(torch.float32).to(torch.float64)
-        rope = rec[:, :, 528:].contiguous().view(torch.bfloat16).to(torch.float64)
-        exact = torch.cat([lat * sc4.repeat_interleave(128, dim=-1), rope], dim=-1)
-    else:
-        codes = inp.kv.view(torch.float8_e4m3fn).to(torch.float64)
-        sc = inp.kv_scales.to(torch.float64)
-        grp = torch.tensor([0] * 128 + [1] * 128 + [2] * 128 + [3] * 128 + [4] * 64)
-        exact = codes * sc[:, :, grp]
-    rounded = exact.to(torch.float16).to(torch.float64)
-    q = inp.q.to(torch.float64)
-    _, l_ex = oracle.mla_decode(q, exact, inp.block_table, inp.seqlens, inp.s_q, inp.softmax_scale,
-                                kv_dtype=oracle.KV_F64, rows=rows)
-    _, l_16 = oracle.mla_decode(q, rounded, inp.block_table, inp.seqlens, inp.s_q, inp.softmax_scale,
-                                kv_dtype=oracle.KV_F64, rows=rows)
-    l_16, l_ex = np.asarray(l_16), np.asarray(l_ex)
-    fin = np.isfinite(l_16) & np.isfinite(l_ex)  # rows with no visible key have lse = -inf
-    d = np.zeros_like(l_ex)
-    d[fin] = np.abs(l_16[fin] - l_ex[fin])
-    return d
-
-
-def compare(out_g, lse_g, out_r, lse_r, tol, lse_extra=None):
-    """Element-wise comparison; returns the measured errors.  `lse_extra`
-    (per row) widens the lse bound by an error the arithmetic cannot avoid
-    (see fp16_k_lse_shift)."""
+def compare(out_g, lse_g, out_r, lse_r, tol):
+    """Element-wise comparison under the stated tolerances (max abs, relative
+    L2, lse abs on every row); returns the measured errors."""
     max_abs_tol, rel_tol, lse_tol = tol
     assert out_g.shape == out_r.shape and lse_g.shape == lse_r.shape
     assert np.isfinite(out_g).all(), "GPU output has NaN/Inf"
@@ -86,9 +54,7 @@ def compare(out_g, lse_g, out_r, lse_r, tol, lse_extra=None):
     rel = float(np.linalg.norm(d) / max(np.linalg.norm(out_r[full]), 1e-30))
     lse_d = np.abs(lse_g[full] - lse_r[full])
     lse_err = float(lse_d.max())
-    bound = lse_tol + (np.asarray(lse_extra)[full] if lse_extra is not None else 0.0)
     assert max_abs <= max_abs_tol, f"max abs error {max_abs} > {max_abs_tol}"
     assert rel <= rel_tol, f"relative L2 error {rel} > {rel_tol}"
-    worst = int(np.argmax(lse_d - bound))
-    assert (lse_d <= bound).all(), f"lse error {float(lse_d[worst])} > {float(np.broadcast_to(bound, lse_d.shape)[worst])}"
+    assert lse_err <= lse_tol, f"lse error {lse_err} > {lse_tol}"
     return max_abs, rel, lse_err

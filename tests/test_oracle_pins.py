@@ -303,12 +303,10 @@ def test_bad_page_id_is_an_error():
         oracle.mla_decode(inp.q, inp.kv, bt, inp.seqlens, 1, inp.softmax_scale)
 
 
-def test_fp8_helper_dequantisation_matches_the_oracle_code_path():
-    """The GPU tests widen the fp8 lse bound per row by the shift that
-    rounding the dequantised cache to fp16 causes (tests/gpu_helpers.py).
-    That helper rebuilds the dequantised cache with torch; with no rounding it
-    must give exactly the oracle's own fp8 result."""
-    from tests.gpu_helpers import fp16_k_lse_shift
+def test_fp8_cache_decodes_like_torch_in_the_oracle():
+    """The oracle's fp8 path (e4m3 codes times the per-token group scales)
+    equals its fp64 path on the cache dequantised independently with torch's
+    float8_e4m3fn decoder, bit for bit."""
     inp = gen.make_inputs("x", seqlens=[70, 5, 1], heads=8, s_q=2, kv_fp8=True, seed=3)
     codes = inp.kv.view(torch.float8_e4m3fn).to(torch.float64)
     grp = torch.tensor([0] * 128 + [1] * 128 + [2] * 128 + [3] * 128 + [4] * 64)
@@ -317,8 +315,6 @@ def test_fp8_helper_dequantisation_matches_the_oracle_code_path():
                                  inp.softmax_scale, kv_dtype=oracle.KV_F64)
     o_c, l_c = oracle.mla_decode_inputs(inp)
     assert np.array_equal(o_f, o_c) and np.array_equal(l_f, l_c)
-    shift = fp16_k_lse_shift(inp)
-    assert shift.shape == l_c.shape and (shift >= 0).all() and shift.max() < 5e-3
 
 
 def test_fp8_variant_b_records_decode_like_torch():
