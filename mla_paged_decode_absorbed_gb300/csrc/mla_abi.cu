@@ -420,6 +420,26 @@ mla_status make_kv_map4(const void* kv, int num_pages, int chunks, CUtensorMap* 
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
+// The bf16 cache as a 5-D tensor (64 channels, 8 tokens, 9 channel chunks, 8
+// token groups, pages) for the scorer: one box (64, 8, 9, 8, 1) is a whole
+// page, landing as token-group-major 1 KB atoms (group g, chunk c at
+// (9g + c) KB, 128-byte swizzled), so the 8-row groups of a page are 9 KB
+// apart and a page in the next 72 KB stage continues the same stride: two
+// adjacent stages are one 128-token MMA operand.
+mla_status make_kv_map5(const void* kv, int num_pages, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  cuuint64_t dims[5] = {64, 8, 9, 8, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[4] = {kDqk * 2, 128, 8 * kDqk * 2, kDqk * 2 * kPage};
+  cuuint32_t box[5] = {64, 8, 9, 8, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
 // fp8 cache as a 4-D byte tensor (64 bytes, 64 tokens, `nchunks` chunks of
 // 64 channels, pages) starting at `base`, with `token_bytes` per token:
 // variant A [P, 64, 576] e4m3 (9 chunks); variant B [P, 64, 656] records
@@ -545,8 +565,9 @@ mla_status run_plan(const Prepared& p, const int32_t* seqlens, cudaStream_t stre
 mla_status run_attention(const Prepared& p, const void* q, const void* kv, const float* kv_scales,
                          const int32_t* bt, const int32_t* seqlens, float scale, void* out, float* lse,
                          cudaStream_t stream) {
-  // page maps of the scorer and the accumulator: bf16, 9 and 8 swizzled
-  // 64-channel blocks; fp8, every raw e4m3 chunk of the row for the scorer
+  // page maps of the scorer and the accumulator: bf16, the whole page
+  // token-group-major (scorer) and 8 chunk-major 64-channel blocks
+  // (accumulator); fp8, every raw e4m3 chunk of the row for the scorer
   // (variant B: the 8 latent chunks, plus the two bf16 RoPE chunks by their
   // own map) and the 8 latent chunks for the accumulator
   CUtensorMap map_s, map_a, map_r;
@@ -565,7 +586,7 @@ mla_status run_attention(const Prepared& p, const void* q, const void* kv, const
           st = make_kv_map_fp8(kv, p.x.P, tb, nch, 1, &map_r);
       }
     } else {
-      st = make_kv_map4(kv, p.x.P, 9, &map_s);
+      st = make_kv_map5(kv, p.x.P, &map_s);
       if (st == MLA_OK) st = make_kv_map4(kv, p.x.P, 8, &map_a);
     }
     if (st != MLA_OK) return st;

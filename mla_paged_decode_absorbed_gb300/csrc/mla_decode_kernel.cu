@@ -101,10 +101,17 @@ constexpr int kSmem = kSmemMax;                    // layout + slack for alignin
 constexpr int kAlignSlack = kSmem - kOffBars - kBarBytes;
 static_assert(kAlignSlack >= 0, "shared memory layout too large");
 
-// TMEM columns.  Scorer: Q (576 16-bit channels) then two S buffers (bf16
-// cache) or kGroupSlots per-group score buffers (fp8 cache).
-constexpr uint32_t kColQ = 0, kColS0 = 288, kColS1 = 352, kColG = 288;
-static_assert(kColG + 64 * kGroupSlots <= 512, "fp8 score slots exceed TMEM");
+// TMEM columns.  Scorer: Q (576 16-bit channels) then three 64-column score
+// slots: one per ring stage (bf16 cache; two adjacent slots hold the scores of
+// a page pair) or the per-group score ring (fp8 cache).
+constexpr uint32_t kColQ = 0, kColG = 288;
+static_assert(kColG + 64 * kGroupSlots <= 512 && kGroupSlots == kStages, "score slots exceed TMEM");
+// bf16 scorer stage layout (5-D page map): token group g (8 tokens), chunk c
+// (64 channels) is the 1 KB 128-byte-swizzled atom at (9g + c) KB, so the
+// 8-row groups of a page are kTokGroupStride apart and the next stage's first
+// group follows the last one: two adjacent stages form one 128-token operand.
+constexpr int kTokGroupStride = 9 * 1024;
+static_assert(kStageS == 8 * kTokGroupStride, "a stage is 8 token groups");
 
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -121,8 +128,6 @@ struct Bars {
   uint64_t q_full;        // scorer: Q written to TMEM (softmax warps, 128)
   uint64_t q_tma;         // scorer: first segment's Q block arrived in ring stages 1-2 (1 + tx)
   uint64_t q_smem_free;   // scorer: that Q block was read, stages 1-2 may take pages (128)
-  uint64_t s_full[2];     // scorer: QK done (commit)
-  uint64_t s_free[2];     // scorer: S read by the softmax (128)
   uint64_t pbuf_free[2];  // scorer: accumulator finished with P tile b (remote, 1)
   uint64_t l_free;        // scorer: accumulator read the row sums (remote, 4)
   uint64_t p_full[2];     // accumulator: P tile + factors arrived (1 + tx)
@@ -139,8 +144,9 @@ struct Bars {
   uint64_t drain;
   uint64_t raw_full[kStages];    // fp8: this CTA's raw e4m3 chunks arrived (1 + tx)
   uint64_t dq_sync;              // fp8: the dequant threads read their raw chunks (128), bounded
-  uint64_t sg_full[kGroupSlots]; // fp8 scorer: QK of one scale group done (commit)
-  uint64_t sg_free[kGroupSlots]; // fp8 scorer: that group's scores read by the softmax (128)
+  uint64_t sg_full[kGroupSlots]; // scorer: scores of a slot written (commit); bf16: slot = stage,
+                                 // fp8: one scale group of the group-score ring
+  uint64_t sg_free[kGroupSlots]; // scorer: that slot read by the softmax (128)
   uint64_t stall;                // never signalled: the wait a test's stall request runs out on
   int abort_flag;
   uint32_t tmem_base;
@@ -337,8 +343,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(smem_u32(&bars->q_tma), 1);
     mbar_init(smem_u32(&bars->q_smem_free), 128);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->s_free[i]), 128);
       mbar_init(smem_u32(&bars->pbuf_free[i]), 1);
       mbar_init(smem_u32(&bars->p_full[i]), 1);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
@@ -476,8 +480,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                   tma_load_4d(smem_u32(dst + kRawOffA), &kv_map_a, 0, 0, 0, pid, fb);
                 }
               } else if (scorer) {
+                // token-group-major: (64 channels, 8 tokens, 9 chunks, 8 token groups, page)
                 mbar_arrive_expect_tx(fb, bytes);
-                tma_load_4d(smem_u32(dst), &kv_map_s, 0, 0, 0, pid, fb);
+                tma_load_5d(smem_u32(dst), &kv_map_s, 0, 0, 0, 0, pid, fb);
               } else {
                 mbar_arrive_expect_tx(fb, bytes);
                 tma_load_4d_hint(smem_u32(dst), &kv_map_a, 0, 0, 0, pid, fb, policy);
@@ -524,21 +529,26 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       if (!mbar_wait(smem_u32(&bars->stall), 0u, abort_flag)) ok = false;
     }
     if (scorer) {
-      // S[b] = Q K^T: 36 steps of K=16 over the 576 channels, A = Q in TMEM.
+      // S = Q K^T: 36 steps of K=16 over the 576 channels, A = Q in TMEM.
+      // bf16 cache: a page in ring stage 0 or 1 is paired with the next page of
+      // the segment (which sits in the next stage) and both are scored by one
+      // N=128 chain into two adjacent slots; an N=64 MMA re-reads its slice of
+      // Q from TMEM as an N=128 one does, so the pair costs about what one page
+      // did.  A page in the last stage goes alone (N=64).
       // fp8 cache: the same steps over the exact e4m3 codes, one MMA chain per
       // scale group (8 steps per latent group of 128 channels, 4 for the RoPE)
       // into the next slot of the group-score ring; the softmax applies the
       // tokens' scales and frees the stage.
       const uint32_t idesc = idesc_f16_f32(128, 64, false, false, !kFp8);
+      const uint32_t idesc2 = idesc_f16_f32(128, 128, false, false, !kFp8);
       uint32_t gj = 0;  // fp8: group-score ring counter over the whole kernel
       while (ok && it.next(s)) {
         if (s.empty) continue;
         if (!mbar_wait(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
         q_ph ^= 1u;
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
-          const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
           if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
-          const uint64_t b0 = smem_desc_sw128(smem_u32(smem + stage * kStageS), 16, 1024);
+          const uint64_t b0 = smem_desc_sw128(smem_u32(smem + stage * kStageS), 16, kFp8 ? 1024 : kTokGroupStride);
           if (kFp8) {
             for (int g = 0; g < kGroups && ok; ++g, ++gj) {
               const uint32_t slot = gj % kGroupSlots, gph = (gj / kGroupSlots) & 1u;
@@ -560,18 +570,35 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             }
             if (!ok) break;
           } else {
-            if (!mbar_wait(smem_u32(&bars->s_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
+            // slot = stage; its use for this page has parity ph, the previous one ph ^ 1
+            const bool pair = stage < kStages - 1 && j + 1 < s.page_hi;
+            bool ready = mbar_wait(smem_u32(&bars->sg_free[stage]), ph ^ 1u, abort_flag);
+            if (pair) {
+              ready = ready && mbar_wait(smem_u32(&bars->kv_full[stage + 1]), ph, abort_flag) &&
+                      mbar_wait(smem_u32(&bars->sg_free[stage + 1]), ph ^ 1u, abort_flag);
+            }
+            if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }  // uniform: the issue ends in __syncwarp
             tc_fence_after();
             if (lane == 0) {
-              const uint32_t dcol = tbase + (sb ? kColS1 : kColS0);
+              const uint32_t dcol = tbase + kColG + 64 * stage;
+              const uint32_t id = pair ? idesc2 : idesc;
 #pragma unroll
               for (int k = 0; k < 36; ++k)
-                mma_ts(dcol, tbase + kColQ + 8 * k, b0 + static_cast<uint64_t>(((k >> 2) * kBox + (k & 3) * 32) >> 4),
-                       idesc, k > 0 ? 1u : 0u);
-              mma_commit(smem_u32(&bars->s_full[sb]));
+                mma_ts(dcol, tbase + kColQ + 8 * k, b0 + static_cast<uint64_t>(((k >> 2) * 1024 + (k & 3) * 32) >> 4),
+                       id, k > 0 ? 1u : 0u);
+              mma_commit(smem_u32(&bars->sg_full[stage]));
               mma_commit(smem_u32(&bars->kv_empty[stage]));
+              if (pair) {
+                mma_commit(smem_u32(&bars->sg_full[stage + 1]));
+                mma_commit(smem_u32(&bars->kv_empty[stage + 1]));
+              }
             }
             __syncwarp();
+            if (pair) {  // the second page of the pair is done too (stage + 1 < kStages: no wrap)
+              ++j;
+              ++t;
+              ++stage;
+            }
           }
           if (++stage == kStages) {
             stage = 0;
@@ -907,15 +934,19 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) x[i] = i < nv ? x[i] * row_scale : -INFINITY;
           } else {
-            if (!mbar_wait(smem_u32(&bars->s_full[sb]), sph, abort_flag)) { ok = false; break; }
+            const uint32_t slot = t % kStages, sph3 = (t / kStages) & 1u;  // the page's stage and its use
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
             uint32_t v0[32], v1[32];
-            const uint32_t col = tbase + lane_off + (sb ? kColS1 : kColS0);
+            const uint32_t col = tbase + lane_off + kColG + 64 * slot;
             tmem_ld32(col, v0);
             tmem_ld32(col + 32, v1);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars->s_free[sb]));
+            mbar_arrive(smem_u32(&bars->sg_free[slot]));
             const int nv = n_vis - j * kPage;  // keys of this page visible to the row
 #pragma unroll
             for (int i = 0; i < 32; ++i) {

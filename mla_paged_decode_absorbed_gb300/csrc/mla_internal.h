@@ -73,10 +73,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int decode_smem_bytes(bool fp8);
 cudaError_t decode_max_active_clusters(bool fp8, int* clusters);
 // kv_map_s / kv_map_a: the page maps of the scorer and the accumulator.  bf16
-// cache: the cache as a 4-D tensor (64 channels, 64 tokens, 9 channel chunks,
-// pages) with a chunk stride of 128 bytes; one box brings chunks 0..8 (scorer)
-// or 0..7 (accumulator) of a page as consecutive 64-token x 64-channel
-// swizzled blocks.  fp8 cache: the e4m3 bytes as a 4-D tensor (64 bytes, 64
+// cache: the scorer's is a 5-D tensor (64 channels, 8 tokens, 9 channel
+// chunks, 8 token groups, pages) whose box is a whole page as token-group-major
+// 1 KB atoms; the accumulator's a 4-D tensor (64 channels, 64 tokens, 9
+// channel chunks, pages) whose box brings chunks 0..7 as consecutive
+// 64-token x 64-channel swizzled blocks.  fp8 cache: the e4m3 bytes as a 4-D tensor (64 bytes, 64
 // tokens, 9 chunks (variant B: 8 latent chunks of a 656-byte record),
 // pages), 64-byte swizzled; boxes of every chunk (scorer) or the 8 latent
 // chunks (accumulator), and kv_map_r the two bf16 RoPE chunks of a variant B
