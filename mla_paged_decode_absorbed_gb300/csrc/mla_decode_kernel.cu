@@ -81,8 +81,8 @@ static_assert(kPartBytes <= kStages * kStageO, "a partial slot must fit in the p
 
 // Shared-memory layout (byte offsets from the 1024-aligned base; the same in
 // both CTAs, each uses its part).  Both CTAs keep their page ring at offset 0.
-constexpr int kQStageBytes = 32 * 64;              // scorer: per softmax warp, 32 rows x 32 channels
-constexpr int kOffQStage = kStages * kStageS;      // scorer: Q transpose staging [4]
+constexpr int kQStageBytes = 32 * 64;              // scorer: Q transpose staging per lane quarter:
+constexpr int kOffQStage = kStages * kStageS;      // bf16, 2 x 1 KB (one per softmax half); fp8, 1 KB
 constexpr int kScorerEnd = kOffQStage + 4 * kQStageBytes;
 // fp8 scorer: a smaller Q staging (32 rows x 16 channels per warp), then the
 // per-stage scale slots the softmax reads
@@ -93,7 +93,13 @@ constexpr int kOffP = kStages * kStageO;           // accumulator: P tiles [2]
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;     // accumulator: rescale factors [2][128]
 constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: (row sum, lse) [128]
 constexpr int kAccEnd = kOffL + kRowsPerBlock * 8;
+// bf16 scorer: each row's softmax runs on two threads (keys 0..31 and 32..63
+// of a page) that exchange their maxima (and at a segment's end their row
+// sums) through [parity][half][row] floats here
+constexpr int kOffXchg = kScorerEnd;
+constexpr int kXchgBytes = 2 * 2 * kRowsPerBlock * 4;
 constexpr int kOffBars = kScorerEnd > kAccEnd ? kScorerEnd : kAccEnd;
+static_assert(kOffXchg + kXchgBytes <= kOffBars, "softmax exchange area overlaps the barriers");
 static_assert(kScorerEndF8 <= kOffBars, "fp8 scorer layout overlaps the barriers");
 constexpr int kBarBytes = 384;
 constexpr int kSmemMax = 232448;
@@ -117,17 +123,21 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Ten warps either way: loader, MMA issuer, four row warps (softmax of the
+// scorer, rescale + epilogue of the accumulator), then four more: the fp8
+// dequantisation, or (bf16 scorer) the second half of each row's softmax.
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kThreads = kFp8 ? 320 : 192;
+  static constexpr int kThreads = 320;
+  static constexpr int kSoftmaxCols = kFp8 ? 64 : 32;  // keys of a page one softmax thread scores
 };
 
 struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t q_full;        // scorer: Q written to TMEM (softmax warps, 128)
+  uint64_t q_full;        // scorer: Q written to TMEM (softmax threads: bf16 256, fp8 128)
   uint64_t q_tma;         // scorer: first segment's Q block arrived in ring stages 1-2 (1 + tx)
-  uint64_t q_smem_free;   // scorer: that Q block was read, stages 1-2 may take pages (128)
+  uint64_t q_smem_free;   // scorer: that Q block was read, stages 1-2 may take pages (256)
   uint64_t pbuf_free[2];  // scorer: accumulator finished with P tile b (remote, 1)
   uint64_t l_free;        // scorer: accumulator read the row sums (remote, 4)
   uint64_t p_full[2];     // accumulator: P tile + factors arrived (1 + tx)
@@ -146,7 +156,8 @@ struct Bars {
   uint64_t dq_sync;              // fp8: the dequant threads read their raw chunks (128), bounded
   uint64_t sg_full[kGroupSlots]; // scorer: scores of a slot written (commit); bf16: slot = stage,
                                  // fp8: one scale group of the group-score ring
-  uint64_t sg_free[kGroupSlots]; // scorer: that slot read by the softmax (128)
+  uint64_t sg_free[kGroupSlots]; // scorer: that slot read by the softmax (fp8: 128; bf16: 256, both halves)
+  uint64_t mx_bar[4];            // bf16 scorer: the two softmax halves of a lane quarter exchanged (64)
   uint64_t stall;                // never signalled: the wait a test's stall request runs out on
   int abort_flag;
   uint32_t tmem_base;
@@ -339,9 +350,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(smem_u32(&bars->kv_full[s]), kFp8 ? 128 : 1);
       mbar_init(smem_u32(&bars->kv_empty[s]), (kFp8 && scorer) ? 128 : 1);
     }
-    mbar_init(smem_u32(&bars->q_full), 128);
+    // bf16: both softmax halves write Q; fp8: the four softmax warps
+    mbar_init(smem_u32(&bars->q_full), kFp8 ? 128 : 256);
     mbar_init(smem_u32(&bars->q_tma), 1);
-    mbar_init(smem_u32(&bars->q_smem_free), 128);
+    mbar_init(smem_u32(&bars->q_smem_free), kFp8 ? 128 : 256);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->pbuf_free[i]), 1);
       mbar_init(smem_u32(&bars->p_full[i]), 1);
@@ -359,8 +371,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars->raw_full[s]), 1);
     for (int s = 0; s < kGroupSlots; ++s) {
       mbar_init(smem_u32(&bars->sg_full[s]), 1);
-      mbar_init(smem_u32(&bars->sg_free[s]), 128);
+      mbar_init(smem_u32(&bars->sg_free[s]), kFp8 ? 128 : 256);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&bars->mx_bar[s]), 64);
     mbar_init(smem_u32(&bars->stall), 1);
     mbar_init(smem_u32(&bars->dq_sync), 128);
     bars->abort_flag = 0;
@@ -571,7 +584,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (!ok) break;
           } else {
             // slot = stage; its use for this page has parity ph, the previous one ph ^ 1
-            const bool pair = stage < kStages - 1 && j + 1 < s.page_hi;
+            // (not in the first ring cycle: the first segment's Q block holds
+            // stages 1-2 until the softmax has read it, so page 1 lands late)
+            const bool pair = stage < kStages - 1 && j + 1 < s.page_hi && t >= static_cast<uint32_t>(kStages);
             bool ready = mbar_wait(smem_u32(&bars->sg_free[stage]), ph ^ 1u, abort_flag);
             if (pair) {
               ready = ready && mbar_wait(smem_u32(&bars->kv_full[stage + 1]), ph, abort_flag) &&
@@ -659,11 +674,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_wait(smem_u32(&bars->drain), 0u, nullptr);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 6 || (!kFp8 && scorer)) {
     const int wq = warp & 3;
     const int L = wq * 32 + lane;  // query row within the block == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const int ctid = tid - 64;     // 0..127
+    const int ctid = tid - 64;     // 0..127 (rows of warps 2-5)
+    // bf16 scorer: half hh of the row's keys (warps 2-5: keys 0..31 of a page,
+    // warps 6-9: keys 32..63); the fp8 softmax runs whole rows on warps 2-5
+    constexpr int kSC = Cfg<kFp8>::kSoftmaxCols;
+    const int hh = kFp8 ? 0 : (warp >= 6 ? 1 : 0);
+    const int c0 = kSC * hh;
     SegIter it = it0;
     Seg s;
     uint32_t t = 0, seg_n = 0;
@@ -680,52 +700,52 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       float qmul = 1.f, qmul_next = 1.f;
       uint32_t gj = 0;  // fp8: group-score ring counter (advances like the MMA warp's)
 
-      // Q rows of this warp (its TMEM lane quarter) -> TMEM, all 576 channels
-      // (the A operand of QK).  The loads are coalesced: per 32-channel step
-      // a warp instruction reads 8 rows x 64 contiguous bytes, and the step
-      // is transposed through a 2 KB shared staging area so that each thread
-      // then holds its own row for tcgen05.st.
-      uint8_t* const qst = smem + kOffQStage + wq * kQStageBytes;
+      // Q rows of this warp (its TMEM lane quarter) -> TMEM (the A operand of
+      // QK).  bf16: the two softmax halves split the 576 channels (288 each);
+      // fp8: load_q_f16 below, whole rows.  The loads are coalesced: per
+      // 16-channel half-step a warp instruction reads 16 rows x 32 contiguous
+      // bytes, and the half-step is transposed through a 1 KB shared staging
+      // area per warp so that each thread then holds its own row for tcgen05.st.
       auto load_q_bf16 = [&](const Seg& sg) {
+        uint8_t* const qsb = smem + kOffQStage + (hh * 4 + wq) * kQStageBytesF8;
         const int r0 = sg.rb * kRowsPerBlock + wq * 32;  // first row of this warp
-        const int rsub = lane >> 2, csub = lane & 3;     // load view: rows rsub + 8i, 16-byte chunk csub
+        const int rsub = lane >> 1, csub = lane & 1;     // load view: rows rsub + 16i, 16-byte chunk csub of 32
         const uint8_t* qb = reinterpret_cast<const uint8_t*>(a.q) + static_cast<size_t>(sg.b) * a.R * (kDqk * 2);
-        bool rv[4];
-        const uint8_t* rp[4];
+        bool rv[2];
+        const uint8_t* rp[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = r0 + rsub + 8 * i;
+        for (int i = 0; i < 2; ++i) {
+          const int r = r0 + rsub + 16 * i;
           rv[i] = r < a.R;
           rp[i] = qb + static_cast<size_t>(rv[i] ? r : 0) * (kDqk * 2) + csub * 16;
         }
-        for (int s0 = 0; s0 < 18; s0 += 6) {
-          uint4 x[24];
+        for (int h0 = 18 * hh; h0 < 18 * hh + 18; h0 += 6) {
+          uint4 x[12];
 #pragma unroll
-          for (int st = 0; st < 6; ++st)
+          for (int u = 0; u < 6; ++u)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              x[4 * st + i] =
-                  rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (s0 + st) * 64)) : make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < 2; ++i)
+              x[2 * u + i] = rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (h0 + u) * 32)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int st = 0; st < 6; ++st) {
-            // staging row rr at rr * 64, its 16-byte chunk c at (c ^ ((rr >> 1) & 3)) (no bank conflicts)
+          for (int u = 0; u < 6; ++u) {
+            // staging row rr at rr * 32, its 16-byte chunk c at (c ^ ((rr >> 2) & 1)) (no bank conflicts)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int rr = rsub + 8 * i;
-              *reinterpret_cast<uint4*>(qst + rr * 64 + ((csub ^ ((rr >> 1) & 3)) << 4)) = x[4 * st + i];
+            for (int i = 0; i < 2; ++i) {
+              const int rr = rsub + 16 * i;
+              *reinterpret_cast<uint4*>(qsb + rr * 32 + ((csub ^ ((rr >> 2) & 1)) << 4)) = x[2 * u + i];
             }
             __syncwarp();
-            uint32_t w[16];
+            uint32_t w[8];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              const uint4 y = *reinterpret_cast<const uint4*>(qst + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4));
-              w[4 * c4 + 0] = y.x;
-              w[4 * c4 + 1] = y.y;
-              w[4 * c4 + 2] = y.z;
-              w[4 * c4 + 3] = y.w;
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const uint4 y = *reinterpret_cast<const uint4*>(qsb + lane * 32 + ((c2 ^ ((lane >> 2) & 1)) << 4));
+              w[4 * c2 + 0] = y.x;
+              w[4 * c2 + 1] = y.y;
+              w[4 * c2 + 2] = y.z;
+              w[4 * c2 + 3] = y.w;
             }
             __syncwarp();
-            tmem_st16(tbase + lane_off + kColQ + 16 * (s0 + st), w);
+            tmem_st8(tbase + lane_off + kColQ + 8 * (h0 + u), w);
           }
         }
         tmem_wait_st();
@@ -821,22 +841,19 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       auto load_q_tma = [&]() -> bool {
         if (!mbar_wait(smem_u32(&bars->q_tma), 0u, abort_flag)) return false;
         const uint8_t* qs_base = smem + kStageS;
-        for (int c2 = 0; c2 < 9; c2 += 3) {
-          uint32_t w[3][32];
+        // chunks 0..4 by the first softmax half, 5..8 by the second
+        for (int c = hh ? 5 : 0; c < (hh ? 9 : 5); ++c) {
+          uint32_t w[32];
+          const int n = 9 * L + c;
 #pragma unroll
-          for (int h = 0; h < 3; ++h) {
-            const int n = 9 * L + c2 + h;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint4 y = *reinterpret_cast<const uint4*>(qs_base + n * 128 + ((k ^ (n & 7)) << 4));
-              w[h][4 * k + 0] = y.x;
-              w[h][4 * k + 1] = y.y;
-              w[h][4 * k + 2] = y.z;
-              w[h][4 * k + 3] = y.w;
-            }
+          for (int k = 0; k < 8; ++k) {
+            const uint4 y = *reinterpret_cast<const uint4*>(qs_base + n * 128 + ((k ^ (n & 7)) << 4));
+            w[4 * k + 0] = y.x;
+            w[4 * k + 1] = y.y;
+            w[4 * k + 2] = y.z;
+            w[4 * k + 3] = y.w;
           }
-#pragma unroll
-          for (int h = 0; h < 3; ++h) tmem_st32(tbase + lane_off + kColQ + 32 * (c2 + h), w[h]);
+          tmem_st32(tbase + lane_off + kColQ + 32 * c, w);
         }
         mbar_arrive(smem_u32(&bars->q_smem_free));  // this thread's reads are in registers
         tmem_wait_st();
@@ -845,6 +862,18 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         return true;
       };
       bool first_q_tma = !kFp8;
+      // bf16: the two halves of a row meet per page to agree on the page's
+      // maximum (and at a segment's end to add their row sums); bounded waits
+      float* const xchg = reinterpret_cast<float*>(smem + kOffXchg);
+      uint32_t xph = 0;
+      auto exchange = [&](float v, float& other) -> bool {
+        xchg[((xph & 1u) * 2 + hh) * kRowsPerBlock + L] = v;
+        mbar_arrive(smem_u32(&bars->mx_bar[wq]));
+        const bool done = mbar_wait(smem_u32(&bars->mx_bar[wq]), xph & 1u, abort_flag);
+        other = xchg[((xph & 1u) * 2 + (hh ^ 1)) * kRowsPerBlock + L];
+        ++xph;
+        return done;
+      };
 
       while (ok && it.next(s)) {
         if (s.empty) continue;  // the accumulator writes its zero output and lse
@@ -868,7 +897,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
-          if (j == max(s.page_lo, s.page_hi - 3)) {
+          if (hh == 0 && j == max(s.page_lo, s.page_hi - 3)) {
             // the next segment's Q row of this thread into L2 (plain prefetches,
             // so the TMA unit stays free for pages)
             SegIter look = it;
@@ -884,14 +913,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 break;
               }
           }
-          float x[64];
+          float x[kSC];
           if (kFp8) {
             // S = sum_g scale[token][g] * S_g, in fp32 from the group-score ring;
             // the tokens' scales are in the scale slot of the tile's stage
             const int stg = static_cast<int>(t % kStages);
             const float* scl = reinterpret_cast<const float*>(smem + kOffScale + stg * kScaleSlotBytes);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = 0.f;
+            for (int i = 0; i < kSC; ++i) x[i] = 0.f;
             for (int g = 0; g < kGroups; ++g, ++gj) {
               const uint32_t slot = gj % kGroupSlots, gph = (gj / kGroupSlots) & 1u;
               // warp-uniform outcome: tcgen05.ld below is a warp-wide instruction
@@ -915,16 +944,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               }
               const float4* sc4 = reinterpret_cast<const float4*>(scl + g * 64);
 #pragma unroll
-              for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 a = sc4[i4], b = sc4[8 + i4];
+              for (int i4 = 0; i4 < kSC / 8; ++i4) {
+                const float4 a = sc4[i4], b = sc4[kSC / 8 + i4];
                 x[4 * i4 + 0] = fmaf(__uint_as_float(v0[4 * i4 + 0]), a.x, x[4 * i4 + 0]);
                 x[4 * i4 + 1] = fmaf(__uint_as_float(v0[4 * i4 + 1]), a.y, x[4 * i4 + 1]);
                 x[4 * i4 + 2] = fmaf(__uint_as_float(v0[4 * i4 + 2]), a.z, x[4 * i4 + 2]);
                 x[4 * i4 + 3] = fmaf(__uint_as_float(v0[4 * i4 + 3]), a.w, x[4 * i4 + 3]);
-                x[32 + 4 * i4 + 0] = fmaf(__uint_as_float(v1[4 * i4 + 0]), b.x, x[32 + 4 * i4 + 0]);
-                x[32 + 4 * i4 + 1] = fmaf(__uint_as_float(v1[4 * i4 + 1]), b.y, x[32 + 4 * i4 + 1]);
-                x[32 + 4 * i4 + 2] = fmaf(__uint_as_float(v1[4 * i4 + 2]), b.z, x[32 + 4 * i4 + 2]);
-                x[32 + 4 * i4 + 3] = fmaf(__uint_as_float(v1[4 * i4 + 3]), b.w, x[32 + 4 * i4 + 3]);
+                x[kSC / 2 + 4 * i4 + 0] = fmaf(__uint_as_float(v1[4 * i4 + 0]), b.x, x[kSC / 2 + 4 * i4 + 0]);
+                x[kSC / 2 + 4 * i4 + 1] = fmaf(__uint_as_float(v1[4 * i4 + 1]), b.y, x[kSC / 2 + 4 * i4 + 1]);
+                x[kSC / 2 + 4 * i4 + 2] = fmaf(__uint_as_float(v1[4 * i4 + 2]), b.z, x[kSC / 2 + 4 * i4 + 2]);
+                x[kSC / 2 + 4 * i4 + 3] = fmaf(__uint_as_float(v1[4 * i4 + 3]), b.w, x[kSC / 2 + 4 * i4 + 3]);
               }
             }
             if (!ok) break;
@@ -932,7 +961,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             mbar_arrive(smem_u32(&bars->kv_empty[stg]));
             const int nv = n_vis - j * kPage;  // keys of this page visible to the row
 #pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = i < nv ? x[i] * row_scale : -INFINITY;
+            for (int i = 0; i < kSC; ++i) x[i] = i < nv ? x[i] * row_scale : -INFINITY;
           } else {
             const uint32_t slot = t % kStages, sph3 = (t / kStages) & 1u;  // the page's stage and its use
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
@@ -940,21 +969,23 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               break;
             }
             tc_fence_after();
-            uint32_t v0[32], v1[32];
-            const uint32_t col = tbase + lane_off + kColG + 64 * slot;
-            tmem_ld32(col, v0);
-            tmem_ld32(col + 32, v1);
+            uint32_t v0[32];
+            tmem_ld32(tbase + lane_off + kColG + 64 * slot + c0, v0);  // this half's 32 keys
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->sg_free[slot]));
-            const int nv = n_vis - j * kPage;  // keys of this page visible to the row
+            const int nv = n_vis - j * kPage - c0;  // keys of this half visible to the row
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              x[i] = i < nv ? __uint_as_float(v0[i]) * row_scale : -INFINITY;
-              x[32 + i] = 32 + i < nv ? __uint_as_float(v1[i]) * row_scale : -INFINITY;
-            }
+            for (int i = 0; i < kSC; ++i) x[i] = i < nv ? __uint_as_float(v0[i]) * row_scale : -INFINITY;
           }
-          const float mt = max64(x);
+          float mt = x[0];
+#pragma unroll
+          for (int i = 1; i < kSC; ++i) mt = fmaxf(mt, x[i]);
+          if (!kFp8) {  // the page's maximum over both halves of the row
+            float other;
+            if (!exchange(mt, other)) { ok = false; break; }
+            mt = fmaxf(mt, other);
+          }
           float alpha = 1.f;
           if (mt > m_ref + kRescaleLog2) {
             if (m_ref != -INFINITY) {
@@ -963,16 +994,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             }
             m_ref = mt;
           }
-          uint32_t pk[32];
+          uint32_t pk[kSC / 2];
           float ps[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) ps[i] = 0.f;
           if (m_ref == -INFINITY) {
 #pragma unroll
-            for (int v = 0; v < 32; ++v) pk[v] = 0u;
+            for (int v = 0; v < kSC / 2; ++v) pk[v] = 0u;
           } else {
 #pragma unroll
-            for (int v = 0; v < 32; ++v) {
+            for (int v = 0; v < kSC / 2; ++v) {
               const float p0 = ex2_approx(x[2 * v] - m_ref);
               const float p1 = ex2_approx(x[2 * v + 1] - m_ref);
               ps[v & 7] += p0 + p1;
@@ -981,26 +1012,34 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
           l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 
-          // P tile t and the factor to the accumulator (its buffer sb must be free)
+          // this thread's part of P tile t (16-byte granules c0/8 ..) and, from
+          // the first half, the row's factor to the accumulator (its buffer sb must be free)
           if (!mbar_wait(smem_u32(&bars->pbuf_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t pbar = sb ? rPfull1 : rPfull0;
           const uint32_t prow = rP + sb * kPBytes + L * 128;
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            st_async_v4_u32(prow + ((cc ^ (L & 7)) << 4), pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3],
-                            pbar);
-          st_async_f32(rAlpha + sb * kVecBytes + L * 4, alpha, pbar);
+          for (int cc = 0; cc < kSC / 8; ++cc)
+            st_async_v4_u32(prow + (((c0 / 8 + cc) ^ (L & 7)) << 4), pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2],
+                            pk[4 * cc + 3], pbar);
+          if (hh == 0) st_async_f32(rAlpha + sb * kVecBytes + L * 4, alpha, pbar);
         }
         if (!ok) break;
 
-        // the row sum and lse go to the accumulator, which writes the outputs
-        const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
-        if (!mbar_wait(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        st_async_v2_f32(rL + L * 8, l, lse_v, rLfull);
-        ++seg_n;
-
-        // Q of the next segment with pages can go in now (its QK overlaps the
-        // accumulator's last PV and epilogue of this one).
+        if (!kFp8) {  // the row sum over both halves
+          float other;
+          if (!exchange(l, other)) { ok = false; break; }
+          l += other;
+        }
+        if (hh == 0) {
+          // the row sum and lse go to the accumulator, which writes the outputs
+          const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+          if (!mbar_wait(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          st_async_v2_f32(rL + L * 8, l, lse_v, rLfull);
+          ++seg_n;
+        }
+        // Q of the next segment with pages can go in now: the QK of this
+        // segment's last page is done (its scores were read), and the next
+        // QK overlaps the accumulator's last PV and epilogue of this one
         {
           SegIter look = it;
           Seg nx;
