@@ -56,6 +56,7 @@ constexpr int kBox = 64 * 64 * 2;                  // 64 tokens x 64 channels, 1
 constexpr int kStages = 3;
 constexpr int kStageS = 9 * kBox;                  // scorer: channels 0..575
 constexpr int kStageO = 8 * kBox;                  // accumulator: channels 0..511
+static_assert(kStageS == 64 * kDqk * 2, "half a Q row block fills one scorer stage");
 // fp8 cache: each CTA TMA-loads the raw e4m3 chunks of every block it needs
 // (64 tokens x 64 bytes each, 64-byte swizzled) into the top of its ring
 // stage and rewrites the stage in place as fp16: the scorer as the exact
@@ -136,8 +137,6 @@ struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t q_full;        // scorer: Q written to TMEM (softmax threads: bf16 256, fp8 128)
-  uint64_t q_tma;         // scorer: first segment's Q block arrived in ring stages 1-2 (1 + tx)
-  uint64_t q_smem_free;   // scorer: that Q block was read, stages 1-2 may take pages (256)
   uint64_t pbuf_free[2];  // scorer: accumulator finished with P tile b (remote, 1)
   uint64_t l_free;        // scorer: accumulator read the row sums (remote, 4)
   uint64_t p_full[2];     // accumulator: P tile + factors arrived (1 + tx)
@@ -352,8 +351,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     // bf16: both softmax halves write Q; fp8: the four softmax warps
     mbar_init(smem_u32(&bars->q_full), kFp8 ? 128 : 256);
-    mbar_init(smem_u32(&bars->q_tma), 1);
-    mbar_init(smem_u32(&bars->q_smem_free), kFp8 ? 128 : 256);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->pbuf_free[i]), 1);
       mbar_init(smem_u32(&bars->p_full[i]), 1);
@@ -430,10 +427,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     SegIter it = it0;
     Seg s;
     const uint64_t policy = l2_policy_evict_first();
-    // bf16 scorer: the first segment's Q block (128 rows x 576 channels =
-    // exactly two ring stages) comes in by TMA right after the first page, into
-    // stages 1-2; pages go there only after the softmax warps have read it.
-    int q_tma_state = (scorer && !kFp8) ? 0 : 2;  // 0: not issued, 1: issued, 2: done
+    // bf16 scorer: each segment's Q block (128 rows x 576 channels, exactly
+    // two ring stages) goes through the ring ahead of the segment's pages, as
+    // two 64-row copies; the softmax warps move it to TMEM, and the MMA warp
+    // frees the two stages once Q is there.  So the next segment's Q arrives
+    // while the current segment still runs.
+    const bool q_ring = scorer && !kFp8;
     // At kernel start every CTA wants its first data at once (DRAM-bound).  The
     // accumulator needs V only for its first PV, after the first P tile has
     // arrived; waiting for that keeps its (second) reads of the first pages
@@ -447,6 +446,26 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     const uint32_t bytes = static_cast<uint32_t>(nbox * kBox);
     while (ok && it.next(s)) {
       if (s.empty) continue;
+      for (int h = 0; q_ring && h < 2; ++h) {
+        if (lane == 0) {
+          if (!mbar_wait(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
+            ok = false;
+            if (!*abort_flag) signal_abort(bars, a.err, peer);
+          } else {
+            const uint32_t qb = smem_u32(&bars->kv_full[stage]);
+            mbar_arrive_expect_tx(qb, static_cast<uint32_t>(kStageS));
+            tma_load_4d(smem_u32(smem + stage * kStageS), &q_map, 0, 0, s.rb * kRowsPerBlock + 64 * h, s.b, qb);
+            last_par[stage] = ph == 0u ? 0 : 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (++stage == kStages) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
       const int32_t* bt = a.block_table + static_cast<size_t>(s.b) * a.max_pages;
       for (int p0 = s.page_lo; ok && p0 < s.page_hi; p0 += 32) {
         const int my_p = p0 + lane;
@@ -457,13 +476,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           if (lane == 0 && wait_first_p) {
             wait_first_p = false;
             if (!mbar_wait<true>(smem_u32(&bars->p_full[0]), 0u, abort_flag)) {
-              ok = false;
-              if (!*abort_flag) signal_abort(bars, a.err, peer);
-            }
-          }
-          if (lane == 0 && ok && q_tma_state == 1) {
-            q_tma_state = 2;
-            if (!mbar_wait(smem_u32(&bars->q_smem_free), 0u, abort_flag)) {
               ok = false;
               if (!*abort_flag) signal_abort(bars, a.err, peer);
             }
@@ -501,14 +513,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 tma_load_4d_hint(smem_u32(dst), &kv_map_a, 0, 0, 0, pid, fb, policy);
               }
               last_par[stage] = static_cast<int>(ph);
-              if (q_tma_state == 0) {
-                q_tma_state = 1;
-                const uint32_t qb = smem_u32(&bars->q_tma);
-                mbar_arrive_expect_tx(qb, static_cast<uint32_t>(kRowsPerBlock * kDqk * 2));
-                // two boxes of 64 rows (72 KB each, the size of a page copy)
-                tma_load_4d(smem_u32(smem + kStageS), &q_map, 0, 0, s.rb * kRowsPerBlock, s.b, qb);
-                tma_load_4d(smem_u32(smem + 2 * kStageS), &q_map, 0, 0, s.rb * kRowsPerBlock + 64, s.b, qb);
-              }
             }
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -525,7 +529,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       for (int i = 0; i < kStages; ++i)
         if (last_par[i] >= 0)
           mbar_wait(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
-      if (q_tma_state >= 1) mbar_wait(smem_u32(&bars->q_tma), 0u, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -555,10 +558,23 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const uint32_t idesc = idesc_f16_f32(128, 64, false, false, !kFp8);
       const uint32_t idesc2 = idesc_f16_f32(128, 128, false, false, !kFp8);
       uint32_t gj = 0;  // fp8: group-score ring counter over the whole kernel
+      // bf16: score slot s is used by the pages that sit in stage s; bit s of
+      // sgp is the parity of its next use (the Q block's stages score nothing)
+      uint32_t sgp = 0;
       while (ok && it.next(s)) {
         if (s.empty) continue;
         if (!mbar_wait(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
         q_ph ^= 1u;
+        if (!kFp8) {
+          // Q is in TMEM, so the two stages that brought it are free
+          for (int h = 0; h < 2; ++h) {
+            if (lane == 0) mbar_arrive(smem_u32(&bars->kv_empty[stage]));
+            if (++stage == kStages) {
+              stage = 0;
+              ph ^= 1u;
+            }
+          }
+        }
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
           const uint64_t b0 = smem_desc_sw128(smem_u32(smem + stage * kStageS), 16, kFp8 ? 1024 : kTokGroupStride);
@@ -583,15 +599,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             }
             if (!ok) break;
           } else {
-            // slot = stage; its use for this page has parity ph, the previous one ph ^ 1
-            // (not in the first ring cycle: the first segment's Q block holds
-            // stages 1-2 until the softmax has read it, so page 1 lands late)
-            const bool pair = stage < kStages - 1 && j + 1 < s.page_hi && t >= static_cast<uint32_t>(kStages);
-            bool ready = mbar_wait(smem_u32(&bars->sg_free[stage]), ph ^ 1u, abort_flag);
+            // slot = stage (a pair: stage and stage + 1, no wrap)
+            const bool pair = stage < kStages - 1 && j + 1 < s.page_hi;
+            bool ready = mbar_wait(smem_u32(&bars->sg_free[stage]), ((sgp >> stage) & 1u) ^ 1u, abort_flag);
             if (pair) {
               ready = ready && mbar_wait(smem_u32(&bars->kv_full[stage + 1]), ph, abort_flag) &&
-                      mbar_wait(smem_u32(&bars->sg_free[stage + 1]), ph ^ 1u, abort_flag);
+                      mbar_wait(smem_u32(&bars->sg_free[stage + 1]), ((sgp >> (stage + 1)) & 1u) ^ 1u, abort_flag);
             }
+            sgp ^= (pair ? 3u : 1u) << stage;
             if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }  // uniform: the issue ends in __syncwarp
             tc_fence_after();
             if (lane == 0) {
@@ -700,57 +715,34 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       float qmul = 1.f, qmul_next = 1.f;
       uint32_t gj = 0;  // fp8: group-score ring counter (advances like the MMA warp's)
 
-      // Q rows of this warp (its TMEM lane quarter) -> TMEM (the A operand of
-      // QK).  bf16: the two softmax halves split the 576 channels (288 each);
-      // fp8: load_q_f16 below, whole rows.  The loads are coalesced: per
-      // 16-channel half-step a warp instruction reads 16 rows x 32 contiguous
-      // bytes, and the half-step is transposed through a 1 KB shared staging
-      // area per warp so that each thread then holds its own row for tcgen05.st.
-      auto load_q_bf16 = [&](const Seg& sg) {
-        uint8_t* const qsb = smem + kOffQStage + (hh * 4 + wq) * kQStageBytesF8;
-        const int r0 = sg.rb * kRowsPerBlock + wq * 32;  // first row of this warp
-        const int rsub = lane >> 1, csub = lane & 1;     // load view: rows rsub + 16i, 16-byte chunk csub of 32
-        const uint8_t* qb = reinterpret_cast<const uint8_t*>(a.q) + static_cast<size_t>(sg.b) * a.R * (kDqk * 2);
-        bool rv[2];
-        const uint8_t* rp[2];
+      // bf16: Q rows -> TMEM (the A operand of QK) from the segment's two Q
+      // stages of the ring (rows 0..63 in the first, 64..127 in the second;
+      // row r, chunk c at line 9r + c of the 128-byte-swizzled box).  The two
+      // softmax halves split the chunks (0..4, 5..8); the MMA warp frees the
+      // stages after q_full.
+      auto load_q_ring = [&](uint32_t r0) -> bool {
+        const uint32_t rq = r0 + (L >= 64 ? 1u : 0u);
+        const uint32_t st = rq % kStages;
+        if (!mbar_wait(smem_u32(&bars->kv_full[st]), (rq / kStages) & 1u, abort_flag)) return false;
+        const uint8_t* qs_base = smem + st * kStageS;
+        const int row = L & 63;
+        for (int c = hh ? 5 : 0; c < (hh ? 9 : 5); ++c) {
+          uint32_t w[32];
+          const int n = 9 * row + c;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = r0 + rsub + 16 * i;
-          rv[i] = r < a.R;
-          rp[i] = qb + static_cast<size_t>(rv[i] ? r : 0) * (kDqk * 2) + csub * 16;
-        }
-        for (int h0 = 18 * hh; h0 < 18 * hh + 18; h0 += 6) {
-          uint4 x[12];
-#pragma unroll
-          for (int u = 0; u < 6; ++u)
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-              x[2 * u + i] = rv[i] ? __ldg(reinterpret_cast<const uint4*>(rp[i] + (h0 + u) * 32)) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int u = 0; u < 6; ++u) {
-            // staging row rr at rr * 32, its 16-byte chunk c at (c ^ ((rr >> 2) & 1)) (no bank conflicts)
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int rr = rsub + 16 * i;
-              *reinterpret_cast<uint4*>(qsb + rr * 32 + ((csub ^ ((rr >> 2) & 1)) << 4)) = x[2 * u + i];
-            }
-            __syncwarp();
-            uint32_t w[8];
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-              const uint4 y = *reinterpret_cast<const uint4*>(qsb + lane * 32 + ((c2 ^ ((lane >> 2) & 1)) << 4));
-              w[4 * c2 + 0] = y.x;
-              w[4 * c2 + 1] = y.y;
-              w[4 * c2 + 2] = y.z;
-              w[4 * c2 + 3] = y.w;
-            }
-            __syncwarp();
-            tmem_st8(tbase + lane_off + kColQ + 8 * (h0 + u), w);
+          for (int k = 0; k < 8; ++k) {
+            const uint4 y = *reinterpret_cast<const uint4*>(qs_base + n * 128 + ((k ^ (n & 7)) << 4));
+            w[4 * k + 0] = y.x;
+            w[4 * k + 1] = y.y;
+            w[4 * k + 2] = y.z;
+            w[4 * k + 3] = y.w;
           }
+          tmem_st32(tbase + lane_off + kColQ + 32 * c, w);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->q_full));
+        return true;
       };
       // fp8 cache: the MMAs run in fp16, so each row is first scaled by a power
       // of two that puts |q| <= 16384 (no overflow; undone on the scores).
@@ -830,38 +822,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         mbar_arrive(smem_u32(&bars->q_full));
         return ldexpf(1.f, k);
       };
-      auto load_q = [&](const Seg& sg) -> float {
-        if (kFp8) return load_q_f16(sg);
-        load_q_bf16(sg);
-        return 1.f;
-      };
-      // bf16, first segment: the Q block was brought into ring stages 1-2 by
-      // TMA (row r, chunk c at line 9r + c of the 128-byte-swizzled box); each
-      // thread reads its row, frees the stages, and writes TMEM.
-      auto load_q_tma = [&]() -> bool {
-        if (!mbar_wait(smem_u32(&bars->q_tma), 0u, abort_flag)) return false;
-        const uint8_t* qs_base = smem + kStageS;
-        // chunks 0..4 by the first softmax half, 5..8 by the second
-        for (int c = hh ? 5 : 0; c < (hh ? 9 : 5); ++c) {
-          uint32_t w[32];
-          const int n = 9 * L + c;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint4 y = *reinterpret_cast<const uint4*>(qs_base + n * 128 + ((k ^ (n & 7)) << 4));
-            w[4 * k + 0] = y.x;
-            w[4 * k + 1] = y.y;
-            w[4 * k + 2] = y.z;
-            w[4 * k + 3] = y.w;
-          }
-          tmem_st32(tbase + lane_off + kColQ + 32 * c, w);
-        }
-        mbar_arrive(smem_u32(&bars->q_smem_free));  // this thread's reads are in registers
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->q_full));
-        return true;
-      };
-      bool first_q_tma = !kFp8;
+      uint32_t rr = 0, sgp = 0;  // bf16: ring index of the next stage, parities of the score slots
       // bf16: the two halves of a row meet per page to agree on the page's
       // maximum (and at a segment's end to add their row sums); bounded waits
       float* const xchg = reinterpret_cast<float*>(smem + kOffXchg);
@@ -885,19 +846,19 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           n_vis = seqlen - a.s_q + r / a.H + 1;
           n_vis = n_vis < 0 ? 0 : (n_vis > seqlen ? seqlen : n_vis);
         }
-        if (first_q_tma) {
-          first_q_tma = false;
-          if (!load_q_tma()) { ok = false; break; }
-          qmul = 1.f;
+        if (kFp8) {
+          qmul = q_loaded ? qmul_next : load_q_f16(s);
         } else {
-          qmul = q_loaded ? qmul_next : load_q(s);
+          if (!q_loaded && !load_q_ring(rr)) { ok = false; break; }
+          rr += 2;  // the Q block's two stages
+          qmul = 1.f;
         }
         q_loaded = 0;
         const float row_scale = a.scale_log2 * qmul;
         float m_ref = -INFINITY, l = 0.f;
-        for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
+        for (int j = s.page_lo; j < s.page_hi; ++j, ++t, ++rr) {
           const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
-          if (hh == 0 && j == max(s.page_lo, s.page_hi - 3)) {
+          if (kFp8 && j == max(s.page_lo, s.page_hi - 3)) {
             // the next segment's Q row of this thread into L2 (plain prefetches,
             // so the TMA unit stays free for pages)
             SegIter look = it;
@@ -963,7 +924,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kSC; ++i) x[i] = i < nv ? x[i] * row_scale : -INFINITY;
           } else {
-            const uint32_t slot = t % kStages, sph3 = (t / kStages) & 1u;  // the page's stage and its use
+            const uint32_t slot = rr % kStages, sph3 = (sgp >> slot) & 1u;  // the page's stage and its use
+            sgp ^= 1u << slot;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
               ok = false;
               break;
@@ -1045,7 +1007,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           Seg nx;
           while (look.next(nx)) {
             if (!nx.empty) {
-              qmul_next = load_q(nx);
+              if (kFp8) {
+                qmul_next = load_q_f16(nx);
+              } else if (!load_q_ring(rr)) {
+                ok = false;
+              }
               q_loaded = 1;
               break;
             }
