@@ -78,7 +78,22 @@ constexpr int kScaleSlotBytes = kGroups * 64 * 4;  // [group][token] fp32, one s
 constexpr int kPBytes = kRowsPerBlock * 64 * 2;    // P tile: 128 rows x 64 keys, SW128 K-major
 constexpr int kVecBytes = kRowsPerBlock * 4;       // one fp32 per row
 constexpr int kPartBytes = kPartChunks * kRowsPerBlock * 16;  // one fp16 partial slot (128 KB)
-static_assert(kPartBytes <= kStages * kStageO, "a partial slot must fit in the page ring");
+// The accumulator's V ring and its P tiles in flight.  bf16: its V reads
+// hit L2 (the scorer read the page shortly before), so two stages cover
+// their latency, and the freed 64 KB hold four P tiles: the scorer may run
+// up to four tiles ahead of PV.  fp8: three stages (each also holds the raw
+// chunks being converted), two P tiles.
+template <bool kFp8>
+struct AccLayout {
+  static constexpr int kStagesA = kFp8 ? 3 : 2;
+  static constexpr int kPBufs = kFp8 ? 2 : 4;
+  static constexpr int kOffP = kStagesA * kStageO;           // P tiles [kPBufs]
+  static constexpr int kOffAlpha = kOffP + kPBufs * kPBytes;  // rescale factors [kPBufs][128]
+  static constexpr int kOffL = kOffAlpha + kPBufs * kVecBytes;  // (row sum, lse) [128]
+  static constexpr int kEnd = kOffL + kRowsPerBlock * 8;
+  static_assert(kPartBytes <= kStagesA * kStageO, "a partial slot must fit in the page ring");
+};
+constexpr int kMaxPBufs = 4;
 
 // Shared-memory layout (byte offsets from the 1024-aligned base; the same in
 // both CTAs, each uses its part).  Both CTAs keep their page ring at offset 0.
@@ -90,10 +105,7 @@ constexpr int kScorerEnd = kOffQStage + 4 * kQStageBytes;
 constexpr int kQStageBytesF8 = 32 * 32;
 constexpr int kOffScale = kOffQStage + 4 * kQStageBytesF8;
 constexpr int kScorerEndF8 = kOffScale + kStages * kScaleSlotBytes;
-constexpr int kOffP = kStages * kStageO;           // accumulator: P tiles [2]
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;     // accumulator: rescale factors [2][128]
-constexpr int kOffL = kOffAlpha + 2 * kVecBytes;   // accumulator: (row sum, lse) [128]
-constexpr int kAccEnd = kOffL + kRowsPerBlock * 8;
+constexpr int kAccEnd = AccLayout<true>::kEnd > AccLayout<false>::kEnd ? AccLayout<true>::kEnd : AccLayout<false>::kEnd;
 // bf16 scorer: each row's softmax runs on two threads (keys 0..31 and 32..63
 // of a page) that exchange their maxima (and at a segment's end their row
 // sums) through [parity][half][row] floats here
@@ -137,13 +149,13 @@ struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t q_full;        // scorer: Q written to TMEM (softmax threads: bf16 256, fp8 128)
-  uint64_t pbuf_free[2];  // scorer: accumulator finished with P tile b (remote, 1)
+  uint64_t pbuf_free[kMaxPBufs];  // scorer: accumulator finished with P tile b (remote, 1)
   uint64_t l_free;        // scorer: accumulator read the row sums (remote, 4)
-  uint64_t p_full[2];     // accumulator: P tile + factors arrived (1 + tx)
-  uint64_t corr_done[2];  // accumulator: O rescaled if needed for tile parity b (128).  Two
-                          // of them: the rescale warps may finish tile t+1 before the MMA
-                          // warp has observed tile t, which would overrun one barrier.
-  uint64_t pv_done[2];    // accumulator: PV of tile with parity b done (commit)
+  uint64_t p_full[kMaxPBufs];     // accumulator: P tile + factors arrived (1 + tx)
+  uint64_t corr_done[kMaxPBufs];  // accumulator: O rescaled if needed for P buffer b (128).  One
+                                  // per P buffer: the rescale warps may run as many tiles ahead
+                                  // of the MMA warp as there are P buffers.
+  uint64_t pv_done[kMaxPBufs];    // accumulator: PV of the tile in P buffer b done (commit)
   uint64_t o_full;        // accumulator: last PV of a segment done (commit)
   uint64_t o_free;        // accumulator: epilogue read O (128)
   uint64_t l_full;        // accumulator: row sums + lse arrived (1 + tx)
@@ -326,6 +338,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                       const __grid_constant__ CUtensorMap kv_map_r,
                       const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap out_map,
                       const __grid_constant__ CUtensorMap out_map4, const DecodeArgs a) {
+  constexpr int kStagesA = AccLayout<kFp8>::kStagesA, kPBufs = AccLayout<kFp8>::kPBufs;
+  constexpr int kOffP = AccLayout<kFp8>::kOffP, kOffAlpha = AccLayout<kFp8>::kOffAlpha, kOffL = AccLayout<kFp8>::kOffL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -351,13 +365,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     // bf16: both softmax halves write Q; fp8: the four softmax warps
     mbar_init(smem_u32(&bars->q_full), kFp8 ? 128 : 256);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxPBufs; ++i) {
       mbar_init(smem_u32(&bars->pbuf_free[i]), 1);
       mbar_init(smem_u32(&bars->p_full[i]), 1);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
+      mbar_init(smem_u32(&bars->corr_done[i]), 128);
     }
-    mbar_init(smem_u32(&bars->corr_done[0]), 128);
-    mbar_init(smem_u32(&bars->corr_done[1]), 128);
     mbar_init(smem_u32(&bars->o_full), 1);
     mbar_init(smem_u32(&bars->o_free), 128);
     mbar_init(smem_u32(&bars->l_free), 4);
@@ -415,6 +428,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
   const int nbox = scorer ? 9 : 8;                 // 64-channel boxes this CTA needs per page
   const int stage_bytes = scorer ? kStageS : kStageO;
+  const int nst = scorer ? kStages : kStagesA;     // ring stages of this CTA
 
   if (warp == 0) {
     // ---------------------------------------------------------------- loader
@@ -460,7 +474,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        if (++stage == kStages) {
+        if (++stage == nst) {
           stage = 0;
           ph ^= 1u;
         }
@@ -517,7 +531,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          if (++stage == kStages) {
+          if (++stage == nst) {
             stage = 0;
             ph ^= 1u;
           }
@@ -526,7 +540,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     if (!ok && lane == 0) {
       // wait (time-bounded only) for the loads already in flight
-      for (int i = 0; i < kStages; ++i)
+      for (int i = 0; i < nst; ++i)
         if (last_par[i] >= 0)
           mbar_wait(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
     }
@@ -600,7 +614,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (!ok) break;
           } else {
             // slot = stage (a pair: stage and stage + 1, no wrap)
-            const bool pair = stage < kStages - 1 && j + 1 < s.page_hi;
+            // (not a segment's first page: the page after it goes to a stage the
+            // segment's Q block frees only once Q is in TMEM)
+            const bool pair = stage < kStages - 1 && j > s.page_lo && j + 1 < s.page_hi;
             bool ready = mbar_wait(smem_u32(&bars->sg_free[stage]), ((sgp >> stage) & 1u) ^ 1u, abort_flag);
             if (pair) {
               ready = ready && mbar_wait(smem_u32(&bars->kv_full[stage + 1]), ph, abort_flag) &&
@@ -643,7 +659,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         if (s.empty) continue;
         const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
-          const uint32_t sb = t & 1u;
+          const uint32_t sb = t % kPBufs;
           if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageO;
           if (!kFp8) {
@@ -651,7 +667,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (valid < kPage) zero_tail_rows(st, valid > 0 ? valid : 0, 8, lane);
             __syncwarp();
           }
-          if (!mbar_wait(smem_u32(&bars->corr_done[sb]), (t >> 1) & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&bars->corr_done[sb]), (t / kPBufs) & 1u, abort_flag)) { ok = false; break; }
           if (j == s.page_lo) {
             if (!mbar_wait(smem_u32(&bars->o_free), ofree_ph ^ 1u, abort_flag)) { ok = false; break; }
             ofree_ph ^= 1u;
@@ -676,7 +692,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (j + 1 == s.page_hi) mma_commit(smem_u32(&bars->o_full));
           }
           __syncwarp();
-          if (++stage == kStages) {
+          if (++stage == kStagesA) {
             stage = 0;
             ph ^= 1u;
           }
@@ -708,8 +724,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const uint32_t rP = mapa_shared(smem_u32(smem + kOffP), peer);
       const uint32_t rAlpha = mapa_shared(smem_u32(smem + kOffAlpha), peer);
       const uint32_t rL = mapa_shared(smem_u32(smem + kOffL), peer);
-      const uint32_t rPfull0 = mapa_shared(smem_u32(&bars->p_full[0]), peer);
-      const uint32_t rPfull1 = mapa_shared(smem_u32(&bars->p_full[1]), peer);
+      const uint32_t rPfull0 = mapa_shared(smem_u32(&bars->p_full[0]), peer);  // + 8 b: P buffer b's
       const uint32_t rLfull = mapa_shared(smem_u32(&bars->l_full), peer);
       uint32_t q_loaded = 0;
       float qmul = 1.f, qmul_next = 1.f;
@@ -857,7 +872,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         const float row_scale = a.scale_log2 * qmul;
         float m_ref = -INFINITY, l = 0.f;
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t, ++rr) {
-          const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
+          const uint32_t sb = t % kPBufs, sph = (t / kPBufs) & 1u;
           if (kFp8 && j == max(s.page_lo, s.page_hi - 3)) {
             // the next segment's Q row of this thread into L2 (plain prefetches,
             // so the TMA unit stays free for pages)
@@ -977,7 +992,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           // this thread's part of P tile t (16-byte granules c0/8 ..) and, from
           // the first half, the row's factor to the accumulator (its buffer sb must be free)
           if (!mbar_wait(smem_u32(&bars->pbuf_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
-          const uint32_t pbar = sb ? rPfull1 : rPfull0;
+          const uint32_t pbar = rPfull0 + 8u * sb;
           const uint32_t prow = rP + sb * kPBytes + L * 128;
 #pragma unroll
           for (int cc = 0; cc < kSC / 8; ++cc)
@@ -1023,8 +1038,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const float* alpha_s = reinterpret_cast<const float*>(smem + kOffAlpha);
       const float2* l_s = reinterpret_cast<const float2*>(smem + kOffL);
       const uint32_t rLfree = mapa_shared(smem_u32(&bars->l_free), peer);
-      const uint32_t rPfree0 = mapa_shared(smem_u32(&bars->pbuf_free[0]), peer);
-      const uint32_t rPfree1 = mapa_shared(smem_u32(&bars->pbuf_free[1]), peer);
+      const uint32_t rPfree0 = mapa_shared(smem_u32(&bars->pbuf_free[0]), peer);  // + 8 b: P buffer b's
       uint32_t ofull_ph = 0, epi_ph = 0, mrg_n = 0;
       auto epi_sync = [&]() -> bool {
         mbar_arrive(smem_u32(&bars->epi_bar));
@@ -1045,13 +1059,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           continue;
         }
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
-          const uint32_t sb = t & 1u, sph = (t >> 1) & 1u;
+          const uint32_t sb = t % kPBufs, sph = (t / kPBufs) & 1u;
           if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->p_full[sb]), kPBytes + kVecBytes);
           if (!mbar_wait<true>(smem_u32(&bars->p_full[sb]), sph, abort_flag)) { ok = false; break; }
           const float alpha = alpha_s[sb * kRowsPerBlock + L];
           if (__any_sync(0xffffffffu, alpha != 1.f) && j > s.page_lo) {
             // O must hold PV of the previous tile before it is rescaled
-            const uint32_t pb = (t - 1u) & 1u, pph = ((t - 1u) >> 1) & 1u;
+            const uint32_t pb = (t - 1u) % kPBufs, pph = ((t - 1u) / kPBufs) & 1u;
             if (!mbar_wait(smem_u32(&bars->pv_done[pb]), pph, abort_flag)) { ok = false; break; }
             tc_fence_after();
             for (int ch = 0; ch < 16; ++ch) {
@@ -1117,7 +1131,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         tc_fence_after();
         // Final rows go through the P buffer of the segment's last tile (its PV
         // is done; its credit goes back to the scorer only after this).
-        const uint32_t last_sb = (t - 1u) & 1u;
+        const uint32_t last_sb = (t - 1u) % kPBufs;
         uint8_t* const est = smem + kOffP + last_sb * kPBytes + wq * (kPBytes / 4);
         if (mode == 1) {
           // fp16 partial O / l, scaled by a power of two that puts the row's
@@ -1312,7 +1326,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         tc_fence_before();
         if (!epi_sync()) { ok = false; break; }  // all four warps are done with the staging buffer
         if (ctid == 0) {
-          mbar_arrive_remote(last_sb ? rPfree1 : rPfree0);
+          mbar_arrive_remote(rPfree0 + 8u * last_sb);
           if (mode == 1 && k <= kFuseMax) st_release_gpu(a.slot_ready + s.slot, 1);
         }
         mbar_arrive(smem_u32(&bars->o_free));
@@ -1478,7 +1492,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         if (out_of_range) atomicOr(a.err, kErrRange);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&bars->kv_full[stage]));
-        if (++stage == kStages) {
+        if (++stage == nst) {
           stage = 0;
           ph ^= 1u;
         }
