@@ -951,18 +951,25 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->sg_free[slot]));
+            // raw scores (the scale is applied in the exponent's FMA below);
+            // keys the row does not see (only on a request's last pages) -> -inf
             const int nv = n_vis - j * kPage - c0;  // keys of this half visible to the row
 #pragma unroll
-            for (int i = 0; i < kSC; ++i) x[i] = i < nv ? __uint_as_float(v0[i]) * row_scale : -INFINITY;
+            for (int i = 0; i < kSC; ++i) x[i] = __uint_as_float(v0[i]);
+            if (__any_sync(0xffffffffu, nv < kSC)) {
+#pragma unroll
+              for (int i = 0; i < kSC; ++i) x[i] = i < nv ? x[i] : -INFINITY;
+            }
           }
           float mt = x[0];
 #pragma unroll
           for (int i = 1; i < kSC; ++i) mt = fmaxf(mt, x[i]);
-          if (!kFp8) {  // the page's maximum over both halves of the row
+          if (!kFp8) {  // the page's maximum over both halves of the row, then scaled
             float other;
             if (!exchange(mt, other)) { ok = false; break; }
-            mt = fmaxf(mt, other);
+            mt = fmaxf(mt, other) * row_scale;  // softmax_scale > 0: the maximum commutes with it
           }
+          const float xs = kFp8 ? 1.f : row_scale;  // fp8: x is already scaled
           float alpha = 1.f;
           if (mt > m_ref + kRescaleLog2) {
             if (m_ref != -INFINITY) {
@@ -981,8 +988,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           } else {
 #pragma unroll
             for (int v = 0; v < kSC / 2; ++v) {
-              const float p0 = ex2_approx(x[2 * v] - m_ref);
-              const float p1 = ex2_approx(x[2 * v + 1] - m_ref);
+              const float p0 = ex2_approx(fmaf(x[2 * v], xs, -m_ref));
+              const float p1 = ex2_approx(fmaf(x[2 * v + 1], xs, -m_ref));
               ps[v & 7] += p0 + p1;
               pk[v] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
