@@ -322,12 +322,17 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint16_t v) {
 }
 
 // Tree reductions over 64 values (independent chains for ILP).
-__device__ __forceinline__ float max64(const float (&x)[64]) {
-  float m[8];
+// Maximum of n floats: two independent chains of three-input maxima.
+template <int n>
+__device__ __forceinline__ float max_n(const float (&x)[n]) {
+  static_assert(n >= 8 && n % 4 == 0, "max_n expects a multiple of four");
+  float m0 = fmax3(x[0], x[1], x[2]), m1 = fmax3(x[3], x[4], x[5]);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(fmaxf(fmaxf(x[8 * i], x[8 * i + 1]), fmaxf(x[8 * i + 2], x[8 * i + 3])),
-                                           fmaxf(fmaxf(x[8 * i + 4], x[8 * i + 5]), fmaxf(x[8 * i + 6], x[8 * i + 7])));
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int i = 6; i + 3 < n; i += 4) {
+    m0 = fmax3(m0, x[i], x[i + 1]);
+    m1 = fmax3(m1, x[i + 2], x[i + 3]);
+  }
+  return fmax3(m0, m1, fmax3(x[n - 2], x[n - 1], x[n - 2]));
 }
 
 // kRopeB (with kFp8): fp8 variant B, 656-byte token records (scales inside,
@@ -961,9 +966,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               for (int i = 0; i < kSC; ++i) x[i] = i < nv ? x[i] : -INFINITY;
             }
           }
-          float mt = x[0];
-#pragma unroll
-          for (int i = 1; i < kSC; ++i) mt = fmaxf(mt, x[i]);
+          float mt = max_n(x);
           if (!kFp8) {  // the page's maximum over both halves of the row, then scaled
             float other;
             if (!exchange(mt, other)) { ok = false; break; }
@@ -1065,10 +1068,25 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
           continue;
         }
+        // A piece of a split unit with at most kFuseMax pieces takes its ticket
+        // when its last P tile arrives (the order in which the unit's pieces
+        // near their end); the atomic's result is first needed in the
+        // epilogue, so nothing waits on it.  The piece with the last ticket
+        // merges, after the others have written their partials (it waits on
+        // their flags; they are on their last tile and wait on nothing).
+        int split_first = 0, split_c0 = 0, split_k = 1, ticket = 0;
+        if (s.split) {
+          const int p0 = __ldg(a.pre + s.u), p1 = __ldg(a.pre + s.u + 1);
+          split_first = p0 + a.overhead;
+          split_c0 = split_first / W;
+          split_k = (p1 - 1) / W - split_c0 + 1;
+        }
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t % kPBufs, sph = (t / kPBufs) & 1u;
           if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->p_full[sb]), kPBytes + kVecBytes);
           if (!mbar_wait<true>(smem_u32(&bars->p_full[sb]), sph, abort_flag)) { ok = false; break; }
+          if (j + 1 == s.page_hi && s.split && split_k <= kFuseMax && ctid == 0)
+            ticket = atomicAdd(a.unit_cnt + split_c0, 1);
           const float alpha = alpha_s[sb * kRowsPerBlock + L];
           if (__any_sync(0xffffffffu, alpha != 1.f) && j > s.page_lo) {
             // O must hold PV of the previous tile before it is rescaled
@@ -1103,19 +1121,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->l_full), kRowsPerBlock * 8);
         if (!mbar_wait<true>(smem_u32(&bars->l_full), seg_n & 1u, abort_flag)) { ok = false; break; }
         const float2 lrow = l_s[L];  // (row sum, lse) of this piece
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(rLfree);
         ++seg_n;
         const float l = lrow.x, lse_own = lrow.y;
-        int mode = 0, c0 = 0, k = 1, first = 0;
+        int mode = 0;
+        const int c0 = split_c0, k = split_k, first = split_first;
         if (s.split) {
-          const int p0 = __ldg(a.pre + s.u), p1 = __ldg(a.pre + s.u + 1);
-          first = p0 + a.overhead;
-          c0 = first / W;
-          k = (p1 - 1) / W - c0 + 1;
           mode = 1;
           if (k <= kFuseMax) {
-            if (ctid == 0) bars->ticket = atomicAdd(a.unit_cnt + c0, 1);
+            if (ctid == 0) bars->ticket = ticket;
             if (!epi_sync()) { ok = false; break; }
             if (*reinterpret_cast<volatile int*>(&bars->ticket) == k - 1) mode = 2;
           }
@@ -1176,6 +1189,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                              pack_f16x2(__uint_as_float(o[8 * q + 4]) * f, __uint_as_float(o[8 * q + 5]) * f),
                              pack_f16x2(__uint_as_float(o[8 * q + 6]) * f, __uint_as_float(o[8 * q + 7]) * f));
           }
+          // O has been read and the last tile's P buffer is not used here: the
+          // next segment's PV may start while the stores drain
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars->o_free));
+          if (ctid == 0) mbar_arrive_remote(rPfree0 + 8u * last_sb);
           reinterpret_cast<float2*>(a.lse_part)[static_cast<size_t>(s.slot) * kRowsPerBlock + L] = make_float2(lse_own, sc);
           __threadfence();  // the partial is visible GPU-wide before its ready flag
         } else if (mode == 0) {
@@ -1203,58 +1221,37 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
           if (row_valid) a.lse[out_row] = lse_own;
         } else {
-          // wait for the other pieces' partials (they hold tickets, so they are
-          // in their epilogues and never wait on anything outside their cluster)
-          if (ctid == 0) {
-            for (int i = 0; i < k; ++i)
-              if (c0 + i != c && !wait_flag_gpu(a.slot_ready + piece_slot(i))) atomicOr(a.err, kErrTimeout);
-          }
-          if (!epi_sync()) { ok = false; break; }
-          // lse_total = ln(sum_i exp(lse_i)); out = sum_i exp(lse_i - lse_total) * out_i,
-          // with out_own = O / l and out_i = stored_i * scale_i
-          float lse_i[kFuseMax], sc_i[kFuseMax];
-          float mx = lse_own;
-#pragma unroll
-          for (int i = 0; i < kFuseMax; ++i) {
-            lse_i[i] = -INFINITY;
-            sc_i[i] = 0.f;
-            if (i < k && c0 + i != c) {
-              const float2 ls = __ldcg(reinterpret_cast<const float2*>(a.lse_part) +
-                                       static_cast<size_t>(piece_slot(i)) * kRowsPerBlock + L);
-              lse_i[i] = ls.x;
-              sc_i[i] = ls.y;
-            }
-            mx = fmaxf(mx, lse_i[i]);
-          }
-          float c_own = 0.f, c_i[kFuseMax], lse_tot = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < kFuseMax; ++i) c_i[i] = 0.f;
-          if (mx != -INFINITY) {
-            const float e_own = ex2_approx((lse_own - mx) * kLog2e);
-            float sum = e_own;
-#pragma unroll
-            for (int i = 0; i < kFuseMax; ++i) {
-              c_i[i] = ex2_approx((lse_i[i] - mx) * kLog2e);
-              sum += c_i[i];
-            }
-            const float inv = 1.f / sum;
-#pragma unroll
-            for (int i = 0; i < kFuseMax; ++i) c_i[i] *= inv * sc_i[i];
-            c_own = l > 0.f ? e_own * inv / l : 0.f;
-            lse_tot = mx + lg2_approx(sum) * kLn2;
-          }
-          // At the cluster's last segment the page ring is idle: each other
-          // piece's partial (128 KB) comes in with one round of bulk copies and
-          // is read from shared memory.  Otherwise it is read from global
-          // memory directly.  With several other pieces, the running result
-          // is kept in O (TMEM) between passes.
+          // Incremental LSE merge: one other piece per pass, each pass as soon
+          // as that piece's partial is ready, the unit's pieces taken from its
+          // tail (later pieces start their clusters, so they finish first).
+          // Running result out_run (O times a factor, in TMEM between passes)
+          // and lse_run, starting from the own piece: O / l and lse_own.  With
+          // partial j (lse_j, stored values times sc_j):
+          //   m = max(lse_run, lse_j), e_r = exp(lse_run - m), e_j = exp(lse_j - m),
+          //   out_run <- (e_r out_run + e_j sc_j stored_j) / (e_r + e_j),
+          //   lse_run <- m + ln(e_r + e_j).
+          // (The other pieces hold tickets: they are on their last tile or in
+          // their epilogues and wait on nothing outside their cluster.)
+          float lse_run = lse_own;
+          float o_scale = l > 0.f ? 1.f / l : 0.f;  // O / l is the own piece's result
           const int own = c - c0;
           for (int pi = 0; pi < k - 1 && ok; ++pi) {
-            const int i = pi < own ? pi : pi + 1;
-            float cf = 0.f;
-#pragma unroll
-            for (int x = 0; x < kFuseMax; ++x)
-              if (x == i) cf = c_i[x];
+            const int cand = k - 1 - pi;
+            const int i = cand > own ? cand : cand - 1;  // k-1, ..., 0 without own
+            if (ctid == 0 && !wait_flag_gpu(a.slot_ready + piece_slot(i))) atomicOr(a.err, kErrTimeout);
+            if (!epi_sync()) { ok = false; break; }  // partial i is complete and visible
+            const float2 ls = __ldcg(reinterpret_cast<const float2*>(a.lse_part) +
+                                     static_cast<size_t>(piece_slot(i)) * kRowsPerBlock + L);
+            const float mm = fmaxf(lse_run, ls.x);
+            float a_run = 0.f, cf = 0.f;  // factors on the running result and on the stored partial
+            if (mm != -INFINITY) {
+              const float er = ex2_approx((lse_run - mm) * kLog2e), ej = ex2_approx((ls.x - mm) * kLog2e);
+              const float inv = 1.f / (er + ej);
+              a_run = er * inv * o_scale;
+              cf = ej * inv * ls.y;
+              lse_run = mm + lg2_approx(er + ej) * kLn2;
+            }
+            o_scale = 1.f;
             const uint4* gsrc = reinterpret_cast<const uint4*>(a.o_part) +
                                 static_cast<size_t>(piece_slot(i)) * kPartChunks * kRowsPerBlock;
             const uint4* src = gsrc + L;
@@ -1269,7 +1266,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               ++mrg_n;
               src = reinterpret_cast<const uint4*>(smem) + L;
             }
-            const bool first_pass = pi == 0, last_pass = pi == k - 2;
+            const bool last_pass = pi == k - 2;
             for (int cc = 0; cc < 8; ++cc) {
               float v[64];
               {
@@ -1277,11 +1274,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                 tmem_ld32(tbase + lane_off + 64 * cc, o0);
                 tmem_ld32(tbase + lane_off + 64 * cc + 32, o1);
                 tmem_wait_ld();
-                const float m = first_pass ? c_own : 1.f;
 #pragma unroll
                 for (int x = 0; x < 32; ++x) {
-                  v[x] = __uint_as_float(o0[x]) * m;
-                  v[32 + x] = __uint_as_float(o1[x]) * m;
+                  v[x] = __uint_as_float(o0[x]) * a_run;
+                  v[32 + x] = __uint_as_float(o1[x]) * a_run;
                 }
               }
               uint4 w[8];
@@ -1323,7 +1319,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             if (ring_free && !last_pass && !epi_sync()) { ok = false; break; }  // ring read before the next copy
           }
           if (!ok) break;
-          if (row_valid) a.lse[out_row] = lse_tot;
+          if (row_valid) a.lse[out_row] = lse_run;
           if (ctid == 0) {  // leave the flags and the counter clear for the next call
             for (int i = 0; i < k; ++i)
               if (c0 + i != c) a.slot_ready[piece_slot(i)] = 0;
@@ -1331,12 +1327,18 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
         tc_fence_before();
-        if (!epi_sync()) { ok = false; break; }  // all four warps are done with the staging buffer
-        if (ctid == 0) {
-          mbar_arrive_remote(rPfree0 + 8u * last_sb);
-          if (mode == 1 && k <= kFuseMax) st_release_gpu(a.slot_ready + s.slot, 1);
+        // mode 1: every thread's partial is fenced before the flag; otherwise
+        // all four warps are done with the staging buffer and with O
+        if (!epi_sync()) { ok = false; break; }
+        if (mode == 1) {
+          if (ctid == 0 && k <= kFuseMax) st_release_gpu(a.slot_ready + s.slot, 1);
+        } else {
+          mbar_arrive(smem_u32(&bars->o_free));
+          if (ctid == 0) mbar_arrive_remote(rPfree0 + 8u * last_sb);
         }
-        mbar_arrive(smem_u32(&bars->o_free));
+        // the row sums were read long ago (a remote arrive stalls its thread
+        // for about a microsecond, so it comes last)
+        if (lane == 0) mbar_arrive_remote(rLfree);
       }
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
