@@ -67,7 +67,9 @@ def load_peaks():
 KERNEL_SOURCES = ("mla_paged_decode_absorbed_gb300/csrc/mla_decode_kernel.cu",
                   "mla_paged_decode_absorbed_gb300/csrc/sm103_ptx.cuh",
                   "mla_paged_decode_absorbed_gb300/csrc/mla_internal.h")
-NCU_SUMMARY = {"decode": "profiles/mla_decode_kernel_B64_H128_ncu_full.md"}
+NCU_SUMMARY = {"decode": "profiles/mla_decode_kernel_B64_H128_ncu_full.md",
+               "mtp": "profiles/mla_decode_kernel_mtp_B128_ncu_full.md",
+               "fp8": "profiles/mla_decode_kernel_fp8_B256_ncu_full.md"}
 
 
 def measured_traffic(workload):
