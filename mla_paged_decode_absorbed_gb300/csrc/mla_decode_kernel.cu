@@ -927,14 +927,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 #pragma unroll
               for (int i4 = 0; i4 < kSC / 8; ++i4) {
                 const float4 a = sc4[i4], b = sc4[kSC / 8 + i4];
-                x[4 * i4 + 0] = fmaf(__uint_as_float(v0[4 * i4 + 0]), a.x, x[4 * i4 + 0]);
-                x[4 * i4 + 1] = fmaf(__uint_as_float(v0[4 * i4 + 1]), a.y, x[4 * i4 + 1]);
-                x[4 * i4 + 2] = fmaf(__uint_as_float(v0[4 * i4 + 2]), a.z, x[4 * i4 + 2]);
-                x[4 * i4 + 3] = fmaf(__uint_as_float(v0[4 * i4 + 3]), a.w, x[4 * i4 + 3]);
-                x[kSC / 2 + 4 * i4 + 0] = fmaf(__uint_as_float(v1[4 * i4 + 0]), b.x, x[kSC / 2 + 4 * i4 + 0]);
-                x[kSC / 2 + 4 * i4 + 1] = fmaf(__uint_as_float(v1[4 * i4 + 1]), b.y, x[kSC / 2 + 4 * i4 + 1]);
-                x[kSC / 2 + 4 * i4 + 2] = fmaf(__uint_as_float(v1[4 * i4 + 2]), b.z, x[kSC / 2 + 4 * i4 + 2]);
-                x[kSC / 2 + 4 * i4 + 3] = fmaf(__uint_as_float(v1[4 * i4 + 3]), b.w, x[kSC / 2 + 4 * i4 + 3]);
+                float* xa = x + 4 * i4;
+                float* xb = x + kSC / 2 + 4 * i4;
+                ffma2(xa[0], xa[1], __uint_as_float(v0[4 * i4 + 0]), __uint_as_float(v0[4 * i4 + 1]), a.x, a.y, xa[0], xa[1]);
+                ffma2(xa[2], xa[3], __uint_as_float(v0[4 * i4 + 2]), __uint_as_float(v0[4 * i4 + 3]), a.z, a.w, xa[2], xa[3]);
+                ffma2(xb[0], xb[1], __uint_as_float(v1[4 * i4 + 0]), __uint_as_float(v1[4 * i4 + 1]), b.x, b.y, xb[0], xb[1]);
+                ffma2(xb[2], xb[3], __uint_as_float(v1[4 * i4 + 2]), __uint_as_float(v1[4 * i4 + 3]), b.z, b.w, xb[2], xb[3]);
               }
             }
             if (!ok) break;
@@ -989,11 +987,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 #pragma unroll
             for (int v = 0; v < kSC / 2; ++v) pk[v] = 0u;
           } else {
+            const float nm = -m_ref;
 #pragma unroll
             for (int v = 0; v < kSC / 2; ++v) {
-              const float p0 = ex2_approx(fmaf(x[2 * v], xs, -m_ref));
-              const float p1 = ex2_approx(fmaf(x[2 * v + 1], xs, -m_ref));
-              ps[v & 7] += p0 + p1;
+              float t0, t1;
+              ffma2(t0, t1, x[2 * v], x[2 * v + 1], xs, xs, nm, nm);
+              const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+              float* acc = ps + 2 * (v & 3);
+              fadd2(acc[0], acc[1], acc[0], acc[1], p0, p1);
               pk[v] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
           }
