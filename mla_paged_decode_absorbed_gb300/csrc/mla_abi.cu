@@ -57,21 +57,35 @@ __device__ __forceinline__ int unit_cost(const int32_t* seqlens, int u, int B, i
   return (n + kPage - 1) / kPage + ovh;
 }
 
-// One CTA: per-unit costs, their exclusive prefix sum `pre`, the per-cluster
-// budget W = ceil(total / G), the first unit each cluster touches, and whether
-// some unit has more than kFuseMax pieces.  Also clears the merge counters and
+// One CTA: per-unit costs laid out on the cost axis (`pre`: unit starts,
+// then the end of the last unit, then the end of each row block's stretch),
+// the per-cluster budget W, the first unit each cluster touches, and the
+// units with more than kFuseMax pieces.  Also clears the merge counters and
 // partial-slot flags the attention kernel uses.
+//
+// Layout: the units of a row block (rb-major order u = rb * B + b) lie back
+// to back.  With several row blocks and at least as many clusters, row
+// block r gets its own Gl = G / n_rb clusters and starts at r * Gl * W, with
+// W = max_r ceil(total_r / Gl): cluster r * Gl + g then covers the same
+// stretch of every request's pages for each r, so the row blocks of a
+// request read each page at about the same time and the second read comes
+// from L2.  Otherwise the row blocks follow each other and W = ceil(total / G).
+constexpr int kMaxRowBlocks = 128;  // s_q <= 16, H <= 1024
+
 __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* seqlens, int B, int s_q, int H,
                                                                 int R, int U, int max_pages, int G, int ovh,
                                                                 int32_t* hdr, int32_t* cl_first, int32_t* pre,
                                                                 int32_t* sync) {
   __shared__ int warp_sum[32];
-  __shared__ int s_total, s_njobs;
+  __shared__ int s_total, s_njobs, s_W;
+  __shared__ int s_rb[kMaxRowBlocks + 1];   // prefix of costs at each row block's first unit
+  __shared__ int s_base[kMaxRowBlocks];     // each row block's start on the cost axis
   // the attention kernel may start its prologue now; it reads the plan only
   // after this grid has completed
   asm volatile("griddepcontrol.launch_dependents;" :::);
   const int tid = threadIdx.x, T = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const int n_rb = U / B;
   if (tid == 0) {
     hdr[kHdrErr] = 0;
     hdr[kHdrStall] = 0;
@@ -109,22 +123,47 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
   }
   __syncthreads();
   const int total = s_total;
-  const int W = max(1, (total + G - 1) / G);
+  const int start = warp_sum[warp] + incl - local;  // prefix of costs at u0
+  {
+    int run = start;
+    for (int u = u0; u < u1; ++u) {
+      if (u % B == 0) s_rb[u / B] = run;
+      run += unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
+    }
+    if (tid == 0) s_rb[n_rb] = total;
+  }
+  __syncthreads();
   if (tid == 0) {
+    const bool lockstep = n_rb > 1 && G >= n_rb;
+    int W = 1;
+    if (lockstep) {
+      const int gl = G / n_rb;
+      for (int r = 0; r < n_rb; ++r) W = max(W, (s_rb[r + 1] - s_rb[r] + gl - 1) / gl);
+      for (int r = 0; r < n_rb; ++r) s_base[r] = r * gl * W;
+    } else {
+      W = max(1, (total + G - 1) / G);
+      for (int r = 0; r < n_rb; ++r) s_base[r] = s_rb[r];
+    }
+    s_W = W;
+    for (int r = 0; r < n_rb; ++r) pre[U + 1 + r] = s_base[r] + s_rb[r + 1] - s_rb[r];
+    pre[U] = s_base[n_rb - 1] + s_rb[n_rb] - s_rb[n_rb - 1];
     hdr[kHdrW] = W;
-    hdr[kHdrTotal] = total;
+    hdr[kHdrTotal] = pre[U];
     hdr[kHdrUnits] = U;
     hdr[kHdrClusters] = G;
     hdr[kHdrOvh] = ovh;
-    pre[U] = total;
   }
+  __syncthreads();
+  const int W = s_W;
   // combine jobs: units of more than kFuseMax pieces, as (unit, first cluster,
   // last cluster, slot of the first piece); at most one per first cluster
   int4* jobs = reinterpret_cast<int4*>(sync + 4 * G);
-  int run = warp_sum[warp] + incl - local;
+  int run = start;
   for (int u = u0; u < u1; ++u) {
-    const int p0 = run, p1 = run + unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
-    run = p1;
+    const int cost = unit_cost(seqlens, u, B, s_q, H, R, max_pages, ovh, err);
+    const int r = u / B;
+    const int p0 = s_base[r] + run - s_rb[r], p1 = p0 + cost;
+    run += cost;
     pre[u] = p0;
     const int cf = (p0 + W - 1) / W, cl = (p1 + W - 1) / W - 1;
     for (int c = cf; c <= cl && c < G; ++c) cl_first[c] = u;
@@ -353,7 +392,7 @@ mla_workspace_layout layout_for(const Dims& x, int G) {
   l.cl_first = off;
   off += align256(sizeof(int32_t) * static_cast<size_t>(G));
   l.pre = off;
-  off += align256(sizeof(int32_t) * (static_cast<size_t>(x.U) + 1));
+  off += align256(sizeof(int32_t) * (static_cast<size_t>(x.U) + 1 + x.n_rb));
   l.sync = off;
   off += align256(sizeof(int32_t) * 8 * static_cast<size_t>(G));
   l.lse_part = off;

@@ -182,6 +182,13 @@ struct Seg {
   int u, b, rb, page_lo, page_hi, split, slot, empty;
 };
 
+// End of unit u's cost range: the next unit's start, except for the last
+// unit of a row block (its row block's stretch may be followed by idle cost;
+// the planner stores each row block's end after pre[U]).
+__device__ __forceinline__ int unit_end(const int32_t* pre, int u, int U, int B) {
+  return (u % B == B - 1) ? __ldg(pre + U + 1 + u / B) : __ldg(pre + u + 1);
+}
+
 // Walks the units of cluster c in order (the partition rule of mla_plan).
 struct SegIter {
   const int32_t* pre;
@@ -194,7 +201,7 @@ struct SegIter {
         u = U;
         return false;
       }
-      const int p1 = __ldg(pre + u + 1);
+      const int p1 = unit_end(pre, u, U, B);
       const int cu = u++;
       const int tiles = p1 - p0 - ovh;
       s.u = cu;
@@ -1077,7 +1084,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         // their flags; they are on their last tile and wait on nothing).
         int split_first = 0, split_c0 = 0, split_k = 1, ticket = 0;
         if (s.split) {
-          const int p0 = __ldg(a.pre + s.u), p1 = __ldg(a.pre + s.u + 1);
+          const int p0 = __ldg(a.pre + s.u), p1 = unit_end(a.pre, s.u, a.U, a.B);
           split_first = p0 + a.overhead;
           split_c0 = split_first / W;
           split_k = (p1 - 1) / W - split_c0 + 1;

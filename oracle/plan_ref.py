@@ -11,13 +11,23 @@ They do not fix a rule, so the plan used here is a plain balanced partition:
 * A unit needs ``tiles_u = ceil(n_max / 64)`` KV pages, where ``n_max`` is the
   number of keys visible to the last row of the block
   (``seqlen - s_q + i_last + 1``, clipped to ``[0, max_pages*64]``).
-* Its cost is ``tiles_u + overhead``; ``pre`` is the exclusive prefix sum of
-  costs and ``W = ceil(total / G)`` the cost per cluster for G clusters.
-* Cluster c owns the cost range ``[c*W, (c+1)*W)``.  The pages of unit u sit at
-  cost ``[pre[u] + overhead, pre[u+1])``; a unit with no pages sits at
-  ``pre[u]``.  A unit whose pages cross a cluster boundary is split; each piece
-  writes a partial result into slot ``2c`` (piece starts at ``c*W``) or
-  ``2c+1`` (otherwise), and the combine step merges the pieces.
+* Its cost is ``tiles_u + overhead``.  The units of one row block are laid
+  out back to back on a cost axis; unit u covers ``[pre[u], end[u])`` with
+  ``end[u] = pre[u] + cost``.  Cluster c owns the cost range
+  ``[c*W, (c+1)*W)``.
+* With several row blocks (``n_rb > 1``) and at least ``n_rb`` clusters, each
+  row block gets its own ``Gl = G // n_rb`` clusters: row block r starts at
+  ``r * Gl * W`` with ``W = max_r ceil(total_r / Gl)``, so cluster
+  ``r * Gl + g`` covers the same stretch of every request's pages for each
+  r, and the row blocks of a request read each page at about the same time
+  (the second read comes from L2).  Clusters past ``n_rb * Gl`` and the end
+  of a row block's stretch stay idle.  Otherwise the row blocks follow each
+  other and ``W = ceil(total / G)``.
+* The pages of unit u sit at cost ``[pre[u] + overhead, end[u])``; a unit
+  with no pages sits at ``pre[u]``.  A unit whose pages cross a cluster
+  boundary is split; each piece writes a partial result into slot ``2c``
+  (piece starts at ``c*W``) or ``2c+1`` (otherwise), and the combine step
+  merges the pieces.
 """
 from __future__ import annotations
 
@@ -48,8 +58,14 @@ class Plan:
     overhead: int
     n_rb: int
     tiles: List[int]
-    pre: List[int]
+    pre: List[int]   # unit starts, then pre[U] = the end of the last unit
     W: int
+    ends: List[int]  # end of each unit's cost range
+
+    @property
+    def rb_ends(self) -> List[int]:
+        """End of each row block's stretch (the end of its last unit)."""
+        return [self.ends[(r + 1) * self.B - 1] for r in range(self.n_rb)]
 
     @property
     def units(self) -> int:
@@ -59,7 +75,7 @@ class Plan:
         """The unit containing cost point c*W (units if the range is past the end)."""
         x = c * self.W
         for u in range(self.units):
-            if self.pre[u] <= x < self.pre[u + 1]:
+            if self.pre[u] <= x < self.ends[u]:
                 return u
         return self.units
 
@@ -68,14 +84,14 @@ class Plan:
         lo_c, hi_c = c * self.W, (c + 1) * self.W
         out = []
         for u in range(self.units):
-            if self.pre[u + 1] <= lo_c or self.pre[u] >= hi_c:
+            if self.ends[u] <= lo_c or self.pre[u] >= hi_c:
                 continue
             b, rb = u % self.B, u // self.B
             if self.tiles[u] == 0:
                 if lo_c <= self.pre[u] < hi_c:
                     out.append(Piece(u, b, rb, 0, 0, False, -1))
                 continue
-            a, e = self.pre[u] + self.overhead, self.pre[u + 1]
+            a, e = self.pre[u] + self.overhead, self.ends[u]
             lo, hi = max(a, lo_c), min(e, hi_c)
             if lo >= hi:
                 continue
@@ -96,12 +112,12 @@ class Plan:
         x = hi_c - 1
         u = None
         for v in range(self.units):
-            if self.pre[v] <= x < self.pre[v + 1]:
+            if self.pre[v] <= x < self.ends[v]:
                 u = v
                 break
         if u is None or self.tiles[u] == 0:
             return None
-        a, e = self.pre[u] + self.overhead, self.pre[u + 1]
+        a, e = self.pre[u] + self.overhead, self.ends[u]
         if not (lo_c <= a <= x and e > hi_c):
             return None
         last = (e - 1) // self.W
@@ -129,8 +145,20 @@ def make_plan(seqlens: Sequence[int], s_q: int, H: int, max_pages: int, G: int, 
     for rb in range(n_rb):
         for b in range(B):
             tiles.append(unit_tiles(int(seqlens[b]), s_q, H, rb, max_pages))
-    pre = [0]
-    for t in tiles:
-        pre.append(pre[-1] + t + overhead)
-    W = (pre[-1] + G - 1) // G
-    return Plan(B, s_q, H, G, overhead, n_rb, tiles, pre, W)
+    totals = [sum(t + overhead for t in tiles[r * B:(r + 1) * B]) for r in range(n_rb)]
+    if n_rb > 1 and G >= n_rb:
+        gl = G // n_rb
+        W = max(1, max((t + gl - 1) // gl for t in totals))
+        base = [r * gl * W for r in range(n_rb)]
+    else:
+        W = max(1, (sum(totals) + G - 1) // G)
+        base = [sum(totals[:r]) for r in range(n_rb)]
+    pre, ends = [], []
+    for r in range(n_rb):
+        x = base[r]
+        for b in range(B):
+            pre.append(x)
+            x += tiles[r * B + b] + overhead
+            ends.append(x)
+    pre.append(ends[-1])
+    return Plan(B, s_q, H, G, overhead, n_rb, tiles, pre, W, ends)

@@ -187,6 +187,30 @@ def test_reference_plan_covers_every_page_once(seed):
     _check_plan(plan_ref.make_plan(seqlens, s_q, H, maxp, G, ovh))
 
 
+def test_reference_plan_runs_row_blocks_in_lockstep():
+    """With several row blocks and at least as many clusters, cluster
+    r * Gl + g covers the same stretch of pages of the same requests for
+    every row block r (whose units have equal page counts here), so the
+    row blocks of a request read each page at about the same time; the
+    clusters past n_rb * Gl get nothing."""
+    for s_q, H, G in ((2, 128, 76), (6, 128, 76), (2, 128, 9), (3, 64, 20)):
+        seqlens = [4096, 2048, 640, 3000 - 3000 % 64, 64]
+        plan = plan_ref.make_plan(seqlens, s_q, H, 64, G, 2)
+        n_rb = plan.n_rb
+        assert n_rb > 1
+        gl = G // n_rb
+        for r in range(n_rb):
+            assert plan.pre[r * plan.B] == r * gl * plan.W
+        for g in range(gl):
+            views = []
+            for r in range(n_rb):
+                views.append([(p.b, p.page_lo, p.page_hi, p.split) for p in plan.pieces(r * gl + g)])
+            assert all(v == views[0] for v in views), (s_q, H, G, g, views)
+        for c in range(n_rb * gl, G):
+            assert plan.pieces(c) == []
+        _check_plan(plan)
+
+
 def test_reference_plan_on_named_workloads():
     from workloads import gen
     for name in ("tiny", "decode", "long"):

@@ -212,7 +212,9 @@ def test_verify_equals_batch_extension_on_gpu():
 # ------------------------------------------------------------------ the plan
 @pytest.mark.parametrize("seqlens,heads,s_q,clusters,ovh", [
     ([37, 130], 16, 1, 0, 0),
-    ([1000, 64, 1, 2500, 130, 0], 128, 2, 9, 3),
+    ([1000, 64, 1, 2500, 130, 0], 128, 2, 9, 3),      # two row blocks, clusters split between them
+    ([1000, 64, 1, 2500, 130, 0], 128, 6, 4, 2),      # six row blocks on four clusters: one after another
+    ([4097, 300, 65], 128, 6, 0, 2),                  # six row blocks, every cluster
     (list(range(1, 4000, 97)), 64, 1, 0, 1),
 ])
 def test_device_plan_equals_reference_plan(seqlens, heads, s_q, clusters, ovh):
@@ -231,8 +233,8 @@ def test_device_plan_equals_reference_plan(seqlens, heads, s_q, clusters, ovh):
     many = sum(1 for u in range(ref.units) if ref.piece_count(u) > FUSE_MAX)
     assert hdr == [0, ref.W, ref.pre[-1], ref.units, G, ref.overhead, many]
     assert w[lay.sync:lay.sync + 12 * G].view(torch.int32).eq(0).all()
-    pre = w[lay.pre:lay.pre + 4 * (ref.units + 1)].view(torch.int32).tolist()
-    assert pre == ref.pre
+    pre = w[lay.pre:lay.pre + 4 * (ref.units + 1 + ref.n_rb)].view(torch.int32).tolist()
+    assert pre == ref.pre + ref.rb_ends
     cl_first = w[lay.cl_first:lay.cl_first + 4 * G].view(torch.int32).tolist()
     assert cl_first == [ref.first_unit(c) for c in range(G)]
 
