@@ -87,7 +87,7 @@ typedef struct {
   int32_t d_v;                /* must be 512 (the latent part of each KV row) */
   int32_t kv_dtype;           /* mla_kv_dtype */
   int32_t max_clusters;       /* optional cap on the number of 2-CTA clusters (0 = what the device holds) */
-  int32_t plan_overhead;      /* optional planner cost per (row block, request) in pages (0 = default 2) */
+  int32_t plan_overhead;      /* optional planner cost per (row block, request) in pages (0 = default 4) */
   int32_t reserved[5];        /* must be 0 */
 } mla_desc;
 

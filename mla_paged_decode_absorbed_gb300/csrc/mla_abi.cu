@@ -38,6 +38,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kCombineChunksPerCta = 4;  // 8-channel chunks of every row per combine CTA
 constexpr int kCombineThreads = 128 * kCombineChunksPerCta;
 constexpr int kCombineJobColumns = 4;     // CTA columns of the combine grid (they stride over jobs)
+constexpr int kCombineBatch = 16;        // partial pieces whose loads a combine thread keeps in flight
 
 // ------------------------------------------------------------------ planner
 // Cost of unit u (row block rb = u / B of request b = u % B): the pages the
@@ -189,15 +190,15 @@ __device__ __forceinline__ void combine_rows(const CombineArgs& a, const float2*
   const int b = u % a.B, rb = u / a.B;
   const int r = rb * kRowsPerBlock + L;
   if (r >= a.R) return;
-  // pieces in batches of 8 (all loads of a batch issued together), with a
+  // pieces in batches of kCombineBatch (all loads of a batch issued together), with a
   // running max across batches
   float mx = -INFINITY, wsum = 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int cb = c; cb <= last; cb += 8) {
-    float2 ls[8];
-    uint4 o[8];
+  for (int cb = c; cb <= last; cb += kCombineBatch) {
+    float2 ls[kCombineBatch];
+    uint4 o[kCombineBatch];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kCombineBatch; ++i) {
       const int cc = cb + i;
       ls[i] = make_float2(-INFINITY, 0.f);
       o[i] = make_uint4(0, 0, 0, 0);
@@ -209,7 +210,7 @@ __device__ __forceinline__ void combine_rows(const CombineArgs& a, const float2*
     }
     float bm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) bm = fmaxf(bm, ls[i].x);
+    for (int i = 0; i < kCombineBatch; ++i) bm = fmaxf(bm, ls[i].x);
     const float m_new = fmaxf(mx, bm);
     if (m_new == -INFINITY) continue;  // no piece saw a key of this row yet
     const float keep = mx == -INFINITY ? 0.f : expf(mx - m_new);
@@ -217,7 +218,7 @@ __device__ __forceinline__ void combine_rows(const CombineArgs& a, const float2*
 #pragma unroll
     for (int h = 0; h < 8; ++h) acc[h] *= keep;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kCombineBatch; ++i) {
       const float w = expf(ls[i].x - m_new);  // 0 for a piece that saw no key of this row
       wsum += w;
       const float ws = w * ls[i].y;

@@ -14,7 +14,7 @@ constexpr int kRowsPerBlock = 128;   // query rows (token-major (i, h)) per work
 constexpr int kGroups = 5;           // fp8 scale groups per token
 constexpr int kFp8bRecord = 656;     // fp8 variant B bytes per token: e4m3 latent, 4 fp32 scales, RoPE bf16
 constexpr int kFp8bScaleOffset = 512, kFp8bRopeOffset = 528;
-constexpr int kDefaultOverhead = 2;  // planner cost per work unit, in pages
+constexpr int kDefaultOverhead = 4;  // planner cost per work unit, in pages
 // A split unit with at most this many pieces is merged inside the attention
 // kernel by the piece that finishes last; units with more pieces are merged by
 // the combine kernel.

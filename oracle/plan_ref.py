@@ -36,6 +36,7 @@ from typing import List, Sequence
 
 PAGE = 64
 ROWS_PER_BLOCK = 128
+DEFAULT_OVERHEAD = 4  # the planner's cost per unit when the descriptor leaves it 0
 
 
 @dataclasses.dataclass(frozen=True)

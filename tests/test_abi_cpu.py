@@ -220,9 +220,9 @@ def test_reference_plan_on_named_workloads():
             g = torch.Generator("cpu").manual_seed(gen.workload_spec(name).seed)
             sl = gen._seqlens_for(name, gen.workload_spec(name).batch, g).tolist()
             maxp = max((s + 63) // 64 for s in sl)
-            plan = plan_ref.make_plan(sl, 1, 128, maxp, 76, 2)
+            plan = plan_ref.make_plan(sl, 1, 128, maxp, 76, plan_ref.DEFAULT_OVERHEAD)
         else:
-            plan = plan_ref.make_plan(inp.seqlens.tolist(), 1, 16, inp.max_pages_per_seq, 76, 2)
+            plan = plan_ref.make_plan(inp.seqlens.tolist(), 1, 16, inp.max_pages_per_seq, 76, plan_ref.DEFAULT_OVERHEAD)
         _check_plan(plan)
 
 

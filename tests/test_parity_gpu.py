@@ -229,7 +229,7 @@ def test_device_plan_equals_reference_plan(seqlens, heads, s_q, clusters, ovh):
     lay = mla.mla_get_workspace_layout(d, G)
     w = ws.cpu()
     hdr = w[lay.header:lay.header + 28].view(torch.int32).tolist()
-    ref = plan_ref.make_plan(seqlens, s_q, heads, inp.max_pages_per_seq, G, ovh or 2)
+    ref = plan_ref.make_plan(seqlens, s_q, heads, inp.max_pages_per_seq, G, ovh or plan_ref.DEFAULT_OVERHEAD)
     many = sum(1 for u in range(ref.units) if ref.piece_count(u) > FUSE_MAX)
     assert hdr == [0, ref.W, ref.pre[-1], ref.units, G, ref.overhead, many]
     assert w[lay.sync:lay.sync + 12 * G].view(torch.int32).eq(0).all()
@@ -349,7 +349,7 @@ def test_merge_in_kernel_and_in_combine(clusters, fp8):
     inp = gen.make_inputs("x", seqlens=seqlens, heads=128, s_q=1, kv_fp8=fp8, seed=40 + clusters)
     d = mla.make_desc(inp.batch, 1, 128, inp.num_pages, inp.max_pages_per_seq, max_clusters=clusters)
     G = mla.mla_num_clusters(d)
-    ref = plan_ref.make_plan(seqlens, 1, 128, inp.max_pages_per_seq, G, 2)
+    ref = plan_ref.make_plan(seqlens, 1, 128, inp.max_pages_per_seq, G, plan_ref.DEFAULT_OVERHEAD)
     counts = {ref.piece_count(u) for u in range(ref.units)}
     assert counts & set(range(2, FUSE_MAX + 1)) or max(counts) > FUSE_MAX, counts
     _check(inp, max_clusters=clusters)
