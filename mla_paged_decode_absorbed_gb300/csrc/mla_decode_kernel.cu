@@ -11,16 +11,18 @@
 //   times a contiguous range of that request's pages, run by a cluster of two
 //   CTAs with different jobs:
 //     - the scorer (cluster rank 0) holds the whole Q block (576 channels) in
-//       TMEM, computes S = Q K^T over each page with tcgen05 into a
-//       double-buffered TMEM S, runs the fp32 online softmax, and streams the
+//       TMEM, computes S = Q K^T over each page with tcgen05 into one of three
+//       TMEM score slots (bf16: two pages per MMA chain where they sit in
+//       adjacent ring stages), runs the fp32 online softmax, and streams the
 //       16-bit P tile plus a per-row rescale factor into the accumulator's
 //       shared memory (st.async, 16.5 KB per page, one direction);
 //     - the accumulator (rank 1) holds the 128 x 512 fp32 output in all 512 of
 //       its TMEM columns and runs O += P V with P read from shared memory, the
 //       (rare) O rescales and the epilogue.
-//   Each CTA TMA-loads the channel boxes of each page it needs into its own
-//   3-stage ring (scorer: 576 channels, accumulator: 512); the second read of
-//   a page comes from L2.
+//   Each CTA TMA-loads each page it needs with one copy into its own ring
+//   (scorer: 576 channels, three stages, each segment's Q block passing
+//   through the same ring; accumulator: 512 channels, two stages for bf16);
+//   the second read of a page comes from L2.
 // * Why this split: a 128 x 512 fp32 accumulator fills a whole SM's TMEM, and
 //   distributed shared memory moves only ~21 bytes per clock per SM pair (as
 //   measured on GB300), so exchanging fp32 partial scores (32 KB per page each
@@ -29,11 +31,12 @@
 // * Roles per CTA: warp 0 loads pages (TMA, 32 block-table entries per read);
 //   warp 1 allocates TMEM and issues the MMAs from one lane; warps 2-5 (one
 //   TMEM lane quarter each, one query row per thread) run the softmax
-//   (scorer) or the rescale and epilogue (accumulator).  The accumulator's PV
-//   commit multicasts the P-buffer credit straight to the scorer's barrier.
-//   The fp8-cache variant has the loader bulk-copy each page's e4m3 bytes into
-//   the top of its ring stage and adds warps 6-9, which rewrite the stage in
-//   place as fp16 (the MMAs then run in fp16).
+//   (scorer) or the rescale and epilogue (accumulator).  The bf16 scorer
+//   splits each row's softmax with warps 6-9 (keys 32..63 of a page).  The
+//   accumulator's PV commit multicasts the P-buffer credit straight to the
+//   scorer's barrier.  The fp8-cache variant has the loader bulk-copy each
+//   page's e4m3 bytes into the top of its ring stage, and warps 6-9 of both
+//   CTAs rewrite the stage in place as fp16 (the MMAs then run in fp16).
 // * Online softmax in base 2 with a lazy rescale: the running max only moves
 //   (and O is only rescaled) when a tile's max exceeds it by more than 8 (a
 //   factor 256); the final division by the row sum is exact either way.  This
@@ -97,8 +100,8 @@ constexpr int kMaxPBufs = 4;
 
 // Shared-memory layout (byte offsets from the 1024-aligned base; the same in
 // both CTAs, each uses its part).  Both CTAs keep their page ring at offset 0.
-constexpr int kQStageBytes = 32 * 64;              // scorer: Q transpose staging per lane quarter:
-constexpr int kOffQStage = kStages * kStageS;      // bf16, 2 x 1 KB (one per softmax half); fp8, 1 KB
+constexpr int kQStageBytes = 32 * 64;              // scorer: 2 KB per lane quarter after the ring
+constexpr int kOffQStage = kStages * kStageS;      // (fp8: the Q staging below; bf16: unused)
 constexpr int kScorerEnd = kOffQStage + 4 * kQStageBytes;
 // fp8 scorer: a smaller Q staging (32 rows x 16 channels per warp), then the
 // per-stage scale slots the softmax reads
