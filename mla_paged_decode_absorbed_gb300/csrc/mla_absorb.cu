@@ -6,9 +6,13 @@
 // D[128 x tt] = A[128 x K] * B[tt x K]^T with tcgen05 (fp32 accumulator in
 // TMEM), where B is tt tokens of the activations (K-major) and A is a 128-row
 // slice of the head's weights (absorb: W_UK rows, K-major; project: W_UV read
-// MN-major).  TMA brings both operands in 64-channel chunks (128-byte swizzle);
-// the epilogue stages D transposed through shared memory so that every
-// (token, head) row of 128 outputs leaves as 256 contiguous bytes.
+// MN-major).  TMA brings each operand in one or two large copies (the TMA
+// unit spends a fixed time per copy, so a few 32-64 KB copies are far faster
+// than many 8 KB ones): the 64-channel chunks of an operand land as
+// consecutive 128-byte-swizzled blocks through a tensor map whose chunk index
+// is a dimension of its own.  The epilogue stages D transposed through shared
+// memory so that every (token, head) row of 128 outputs leaves as 256
+// contiguous bytes.
 //
 // Roofline: the weights (H x 512 x 128 bf16 = 16.8 MB at H = 128) are read
 // once; with few tokens the step is HBM-bound on them, with many it is
@@ -34,17 +38,11 @@ constexpr int kGemmThreads = 128;           // warp 0 loads, warp 1 issues MMAs,
 constexpr int kChunkA = 128 * 64 * 2;       // one 64-channel chunk of a 128-row A tile (16 KB)
 constexpr int kNopeDim = 128, kRopeDim = 64, kLat = 512;
 
-constexpr int kMaxStages = 8;
-constexpr int kStageBudget = 200 * 1024;  // shared memory for the operand stages
-
-// Operand stages: absorb has two K chunks (both in flight); project has
-// eight, as many in flight as fit (8 at 64 tokens, 6 at 128, 4 at 256), so
-// that few rounds of load latency are exposed.
-__host__ __device__ constexpr int gemm_stages(bool project, int tt) {
-  return project ? ((kStageBudget / (kChunkA + tt * 128)) < kMaxStages ? (kStageBudget / (kChunkA + tt * 128))
-                                                                         : kMaxStages)
-                 : 2;
-}
+// Shared memory: A (absorb: 2 chunks x 128 rows = 32 KB; project: 2 halves of
+// 64 output channels x 512 k rows = 128 KB), then B (tt tokens x K).
+// project runs 64-token tiles (B = 64 KB) so that both fit.
+__host__ __device__ constexpr int gemm_a_bytes(bool project) { return project ? 2 * kLat * 128 : 2 * kChunkA; }
+__host__ __device__ constexpr int gemm_b_bytes(bool project, int tt) { return tt * (project ? kLat : kNopeDim) * 2; }
 
 struct GemmArgs {
   const uint16_t* rope;  // absorb: q_rope [T, H, 64] (copied into q[..., 512:576]); project: unused
@@ -65,24 +63,20 @@ template <bool kProject>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mla_absorb_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                            const GemmArgs a) {
-  constexpr int kChunks = kProject ? kLat / 64 : kNopeDim / 64;  // K in 64-channel chunks
-  const int kStages = gemm_stages(kProject, a.tt);               // all chunks in flight when they fit
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tt = a.tt;
-  const int stage_bytes = kChunkA + tt * 128;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* done = empty + kMaxStages;
+  constexpr int kA = gemm_a_bytes(kProject);
+  const int b_bytes = gemm_b_bytes(kProject, tt);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kA + b_bytes);  // [2]: the operand copies landed
+  uint64_t* done = full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int xt = blockIdx.x, h = blockIdx.y, t0 = blockIdx.z * tt;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
-    }
+    mbar_init(smem_u32(&full[0]), 1);
+    mbar_init(smem_u32(&full[1]), 1);
     mbar_init(smem_u32(done), 1);
     fence_mbarrier_init_cluster();
   }
@@ -94,48 +88,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  uint8_t* const sa = smem;
+  uint8_t* const sb = smem + kA;
 
   bool ok = true;
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ loader
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_x);
-    for (int c = 0; c < kChunks && ok; ++c) {
-      const int s = c % kStages;
-      const uint32_t ph = static_cast<uint32_t>(c / kStages) & 1u;
-      if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1u, a.err)) { ok = false; break; }
-      uint8_t* st = smem + s * stage_bytes;
-      const uint32_t fb = smem_u32(&full[s]);
-      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(stage_bytes));
-      if (kProject) {
-        // W_UV[h] rows k = 64c.. (64 of them), output channels j in two 64-wide boxes
-        tma_load_3d(smem_u32(st), &map_w, 0, h * kLat + 64 * c, 0, fb);
-        tma_load_3d(smem_u32(st + kChunkA / 2), &map_w, 64, h * kLat + 64 * c, 0, fb);
-      } else {
-        // W_UK[h] rows n = 128x.. (128 of them), channels k = 64c..
-        tma_load_3d(smem_u32(st), &map_w, 64 * c, h * kLat + 128 * xt, 0, fb);
-      }
-      tma_load_3d(smem_u32(st + kChunkA), &map_x, 64 * c, h, t0, fb);
+    const uint32_t f0 = smem_u32(&full[0]), f1 = smem_u32(&full[1]);
+    if (kProject) {
+      // B: every 64-channel chunk of the tile's tokens (chunk-major), and the
+      // first 256 k rows of W_UV[h] (both 64-wide output-channel halves);
+      // then the other 256 rows on their own barrier
+      mbar_arrive_expect_tx(f0, static_cast<uint32_t>(b_bytes + kA / 2));
+      tma_load_4d(smem_u32(sb), &map_x, 0, t0, 0, h, f0);
+      tma_load_3d(smem_u32(sa), &map_w, 0, h * kLat, 0, f0);
+      mbar_arrive_expect_tx(f1, static_cast<uint32_t>(kA / 2));
+      tma_load_3d(smem_u32(sa + kA / 2), &map_w, 0, h * kLat + 256, 0, f1);
+    } else {
+      // W_UK[h] rows n = 128x.. (both 64-channel chunks) and the tokens' q_nope
+      mbar_arrive_expect_tx(f0, static_cast<uint32_t>(kA + b_bytes));
+      tma_load_3d(smem_u32(sa), &map_w, 0, h * kLat + 128 * xt, 0, f0);
+      tma_load_4d(smem_u32(sb), &map_x, 0, t0, 0, h, f0);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, tt, kProject, false);
-    for (int c = 0; c < kChunks && ok; ++c) {
-      const int s = c % kStages;
-      const uint32_t ph = static_cast<uint32_t>(c / kStages) & 1u;
-      if (!wait_bounded(smem_u32(&full[s]), ph, a.err)) { ok = false; break; }
-      tc_fence_after();
-      uint8_t* st = smem + s * stage_bytes;
-      // A: K-major rows of 128 bytes (absorb), or MN-major 64-channel boxes
-      // 8 KB apart whose rows are k (project); B: K-major token rows.
-      const uint64_t ad = kProject ? smem_desc_sw128(smem_u32(st), kChunkA / 2, 1024)
-                                   : smem_desc_sw128(smem_u32(st), 16, 1024);
-      const uint64_t bd = smem_desc_sw128(smem_u32(st + kChunkA), 16, 1024);
+    // B: K-major token rows, chunk c at c * tt * 128 bytes
+    const uint64_t bd = smem_desc_sw128(smem_u32(sb), 16, 1024);
+    if (kProject) {
+      // A: MN-major, two 64-channel halves 256 rows x 128 B = 32 KB apart (the
+      // descriptor's leading offset) in each 64 KB block of 256 k rows
+      for (int half = 0; half < 2 && ok; ++half) {
+        if (!wait_bounded(smem_u32(&full[half]), 0u, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(smem_u32(sa + half * (kA / 2)), kA / 4, 1024);
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const int kg = 16 * half + k;  // K step of 16 rows: chunk kg / 4 of B
+          mma_ss(tbase, ad + static_cast<uint64_t>((k * 2048) >> 4),
+                 bd + static_cast<uint64_t>(((kg >> 2) * tt * 128 + (kg & 3) * 32) >> 4), idesc, kg > 0 ? 1u : 0u);
+        }
+      }
+    } else {
+      if (wait_bounded(smem_u32(&full[0]), 0u, a.err)) {
+        tc_fence_after();
+        // A: K-major rows of 128 bytes, chunk c at c * 16 KB
+        const uint64_t ad = smem_desc_sw128(smem_u32(sa), 16, 1024);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase, ad + static_cast<uint64_t>((kProject ? k * 2048 : k * 32) >> 4),
-               bd + static_cast<uint64_t>((k * 32) >> 4), idesc, (c > 0 || k > 0) ? 1u : 0u);
-      mma_commit(smem_u32(&empty[s]));
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tbase, ad + static_cast<uint64_t>(((k >> 2) * kChunkA + (k & 3) * 32) >> 4),
+                 bd + static_cast<uint64_t>(((k >> 2) * tt * 128 + (k & 3) * 32) >> 4), idesc, k > 0 ? 1u : 0u);
+      } else {
+        ok = false;
+      }
     }
     if (ok) mma_commit(smem_u32(done));
   }
@@ -191,19 +198,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-int token_tile(int T) { return T <= 64 ? 64 : (T <= 128 ? 128 : 256); }
+int token_tile(bool project, int T) { return project || T <= 64 ? 64 : (T <= 128 ? 128 : 256); }
 
-// stages, alignment slack, barriers (2 x kMaxStages + 1 mbarriers and the TMEM address)
-int gemm_smem(bool project, int tt) { return gemm_stages(project, tt) * (kChunkA + tt * 128) + 1024 + 256; }
-static_assert((2 * kMaxStages + 1) * 8 + 4 <= 256, "barrier block");
+// operands, alignment slack, barriers (3 mbarriers and the TMEM address)
+int gemm_smem(bool project, int tt) { return gemm_a_bytes(project) + gemm_b_bytes(project, tt) + 1024 + 256; }
 
-// bf16 tensor with up to 3 dims (innermost first) as a TMA map with a
-// 64-element x box[1] x box[2] box, 128-byte swizzled.
+// bf16 tensor with up to 4 dims (innermost first) as a TMA map with a
+// 64-element x box[1] x ... box, 128-byte swizzled.  The strides need not
+// grow with the dimension: a dimension of 64-channel chunks (stride 128 B)
+// after a row dimension makes one box land as consecutive swizzled blocks.
 mla_status make_map(const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
                     const cuuint32_t* box, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return MLA_ERR_CUDA;
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
   std::memset(map, 0, sizeof(*map));
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
                    dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -246,20 +254,20 @@ extern "C" mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const
   if (!q_nope || !q_rope || !w_uk || !q || !aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) ||
       !aligned16(q) || (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return MLA_ERR_INVALID_ARG;
-  const int tt = token_tile(tokens);
+  const int tt = token_tile(false, tokens);
   const cuuint64_t H = static_cast<cuuint64_t>(num_heads);
   CUtensorMap mw, mx;
-  {  // W_UK [H*512 rows, 128]: box 64 channels x 128 rows
-    const cuuint64_t dims[3] = {kNopeDim, H * kLat, 1};
-    const cuuint64_t strides[2] = {kNopeDim * 2, H * kLat * kNopeDim * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+  {  // W_UK [H*512 rows n, 128 k] as (64 k, rows, 2 chunks): box 64 x 128 rows x 2 = 32 KB
+    const cuuint64_t dims[3] = {64, H * kLat, 2};
+    const cuuint64_t strides[2] = {kNopeDim * 2, 128};
+    const cuuint32_t box[3] = {64, 128, 2};
     st = make_map(w_uk, 3, dims, strides, box, &mw);
   }
-  if (st == MLA_OK) {  // q_nope [T, H, 128]: box 64 channels x 1 head x tt tokens
-    const cuuint64_t dims[3] = {kNopeDim, H, static_cast<cuuint64_t>(tokens)};
-    const cuuint64_t strides[2] = {kNopeDim * 2, H * kNopeDim * 2};
-    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tt)};
-    st = make_map(q_nope, 3, dims, strides, box, &mx);
+  if (st == MLA_OK) {  // q_nope [T, H, 128] as (64 ch, T, 2 chunks, H): box 64 x tt x 2 x 1
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(tokens), 2, H};
+    const cuuint64_t strides[3] = {H * kNopeDim * 2, 128, kNopeDim * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(tt), 2, 1};
+    st = make_map(q_nope, 4, dims, strides, box, &mx);
   }
   if (st != MLA_OK) return st;
   GemmArgs a;
@@ -279,20 +287,20 @@ extern "C" mla_status mla_project_out(const void* out_latent, const void* w_uv, 
   if (!out_latent || !w_uv || !o || !aligned16(out_latent) || !aligned16(w_uv) || !aligned16(o) ||
       (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return MLA_ERR_INVALID_ARG;
-  const int tt = token_tile(tokens);
+  const int tt = token_tile(true, tokens);
   const cuuint64_t H = static_cast<cuuint64_t>(num_heads);
   CUtensorMap mw, mx;
-  {  // W_UV [H*512 rows k, 128 j]: box 64 j x 64 rows
-    const cuuint64_t dims[3] = {kNopeDim, H * kLat, 1};
-    const cuuint64_t strides[2] = {kNopeDim * 2, H * kLat * kNopeDim * 2};
-    const cuuint32_t box[3] = {64, 64, 1};
+  {  // W_UV [H*512 rows k, 128 j] as (64 j, rows, 2 halves): box 64 x 256 rows x 2 = 64 KB
+    const cuuint64_t dims[3] = {64, H * kLat, 2};
+    const cuuint64_t strides[2] = {kNopeDim * 2, 128};
+    const cuuint32_t box[3] = {64, 256, 2};
     st = make_map(w_uv, 3, dims, strides, box, &mw);
   }
-  if (st == MLA_OK) {  // out [T, H, 512]: box 64 channels x 1 head x tt tokens
-    const cuuint64_t dims[3] = {kLat, H, static_cast<cuuint64_t>(tokens)};
-    const cuuint64_t strides[2] = {kLat * 2, H * kLat * 2};
-    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tt)};
-    st = make_map(out_latent, 3, dims, strides, box, &mx);
+  if (st == MLA_OK) {  // out [T, H, 512] as (64 ch, T, 8 chunks, H): box 64 x 64 tokens x 8 x 1 = 64 KB
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(tokens), 8, H};
+    const cuuint64_t strides[3] = {H * kLat * 2, 128, kLat * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(tt), 8, 1};
+    st = make_map(out_latent, 4, dims, strides, box, &mx);
   }
   if (st != MLA_OK) return st;
   GemmArgs a;
