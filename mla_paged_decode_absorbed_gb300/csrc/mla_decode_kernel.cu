@@ -101,8 +101,13 @@ constexpr int kMaxPBufs = 4;
 // Shared-memory layout (byte offsets from the 1024-aligned base; the same in
 // both CTAs, each uses its part).  Both CTAs keep their page ring at offset 0.
 constexpr int kQStageBytes = 32 * 64;              // scorer: 2 KB per lane quarter after the ring
-constexpr int kOffQStage = kStages * kStageS;      // (fp8: the Q staging below; bf16: unused)
+constexpr int kOffQStage = kStages * kStageS;      // (fp8: the Q staging below; bf16: kOffFwd)
 constexpr int kScorerEnd = kOffQStage + 4 * kQStageBytes;
+// bf16 scorer: the page scores of rows 32..63, forwarded from the warps that
+// can read those TMEM lanes to the warps that run their softmax:
+// [half][4-key group][row] float4 (8 KB, in the otherwise unused Q staging)
+constexpr int kOffFwd = kOffQStage;
+static_assert(kOffFwd + 2 * 8 * 32 * 16 <= kScorerEnd, "forwarding buffer overlaps");
 // fp8 scorer: a smaller Q staging (32 rows x 16 channels per warp), then the
 // per-stage scale slots the softmax reads
 constexpr int kQStageBytesF8 = 32 * 32;
@@ -110,14 +115,14 @@ constexpr int kOffScale = kOffQStage + 4 * kQStageBytesF8;
 constexpr int kScorerEndF8 = kOffScale + kStages * kScaleSlotBytes;
 constexpr int kAccEnd = AccLayout<true>::kEnd > AccLayout<false>::kEnd ? AccLayout<true>::kEnd : AccLayout<false>::kEnd;
 // bf16 scorer: each row's softmax runs on two threads (keys 0..31 and 32..63
-// of a page) that exchange their maxima (and at a segment's end their row
-// sums) through [parity][half][row] floats here
+// of a page) that add their row sums at a segment's end through
+// [parity][half][row] floats here
 constexpr int kOffXchg = kScorerEnd;
 constexpr int kXchgBytes = 2 * 2 * kRowsPerBlock * 4;
 constexpr int kOffBars = kScorerEnd > kAccEnd ? kScorerEnd : kAccEnd;
 static_assert(kOffXchg + kXchgBytes <= kOffBars, "softmax exchange area overlaps the barriers");
 static_assert(kScorerEndF8 <= kOffBars, "fp8 scorer layout overlaps the barriers");
-constexpr int kBarBytes = 384;
+constexpr int kBarBytes = 416;
 constexpr int kSmemMax = 232448;
 constexpr int kSmem = kSmemMax;                    // layout + slack for aligning the base
 constexpr int kAlignSlack = kSmem - kOffBars - kBarBytes;
@@ -139,12 +144,14 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Ten warps either way: loader, MMA issuer, four row warps (softmax of the
-// scorer, rescale + epilogue of the accumulator), then four more: the fp8
-// dequantisation, or (bf16 scorer) the second half of each row's softmax.
+// Warps: loader, MMA issuer, four row warps (softmax of the scorer, rescale +
+// epilogue of the accumulator), then four more: the fp8 dequantisation, or
+// (bf16 scorer) the second half of each row's softmax.  The bf16 variant has
+// two more (warps 10 and 11), which run the softmax of rows 32..63 for the
+// scorer (below); they are idle in the accumulator.
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = kFp8 ? 320 : 384;
   static constexpr int kSoftmaxCols = kFp8 ? 64 : 32;  // keys of a page one softmax thread scores
 };
 
@@ -171,7 +178,10 @@ struct Bars {
   uint64_t sg_full[kGroupSlots]; // scorer: scores of a slot written (commit); bf16: slot = stage,
                                  // fp8: one scale group of the group-score ring
   uint64_t sg_free[kGroupSlots]; // scorer: that slot read by the softmax (fp8: 128; bf16: 256, both halves)
-  uint64_t mx_bar[4];            // bf16 scorer: the two softmax halves of a lane quarter exchanged (64)
+  uint64_t mx_bar[4];            // bf16 scorer: the two softmax halves of a row quarter added their
+                                 // row sums (64)
+  uint64_t fwd_full[2];          // bf16 scorer: half h of rows 32..63's scores forwarded (32)
+  uint64_t fwd_empty[2];         // bf16 scorer: ... and read by both softmax warps of those rows (64)
   uint64_t stall;                // never signalled: the wait a test's stall request runs out on
   int abort_flag;
   uint32_t tmem_base;
@@ -399,6 +409,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(smem_u32(&bars->sg_free[s]), kFp8 ? 128 : 256);
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&bars->mx_bar[s]), 64);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&bars->fwd_full[h]), 32);
+      mbar_init(smem_u32(&bars->fwd_empty[h]), 64);
+    }
     mbar_init(smem_u32(&bars->stall), 1);
     mbar_init(smem_u32(&bars->dq_sync), 128);
     bars->abort_flag = 0;
@@ -721,14 +735,24 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     __syncwarp();
   } else if (warp < 6 || (!kFp8 && scorer)) {
-    const int wq = warp & 3;
-    const int L = wq * 32 + lane;  // query row within the block == TMEM lane
+    // bf16 scorer: a warp can reach only the TMEM lanes of its SM sub-partition
+    // (warp % 4), and the MMA warp (warp 1) shares sub-partition 1 with warps
+    // 5 and 9.  Arithmetic in that sub-partition slows every MMA issue 2-4x
+    // (arithmetic in the other three costs it nothing), so warps 5 and 9 only
+    // move data for rows 32..63: Q into TMEM, and each page's scores from TMEM
+    // to shared memory (`fwd`).  Warps 10 and 11 (sub-partitions 2 and 3) run
+    // the softmax of those rows from there (`xq`).
+    const bool fwd = !kFp8 && scorer && (warp == 5 || warp == 9);
+    const bool xq = !kFp8 && warp >= 10;
+    const int wq = xq ? 1 : (warp & 3);
+    const int L = wq * 32 + lane;  // query row within the block (== TMEM lane, xq: not read)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int ctid = tid - 64;     // 0..127 (rows of warps 2-5)
-    // bf16 scorer: half hh of the row's keys (warps 2-5: keys 0..31 of a page,
-    // warps 6-9: keys 32..63); the fp8 softmax runs whole rows on warps 2-5
+    // bf16 scorer: half hh of the row's keys (warps 2-5 and 10: keys 0..31 of
+    // a page, warps 6-9 and 11: keys 32..63); the fp8 softmax runs whole rows
+    // on warps 2-5
     constexpr int kSC = Cfg<kFp8>::kSoftmaxCols;
-    const int hh = kFp8 ? 0 : (warp >= 6 ? 1 : 0);
+    const int hh = kFp8 ? 0 : (xq ? warp - 10 : (warp >= 6 ? 1 : 0));
     const int c0 = kSC * hh;
     SegIter it = it0;
     Seg s;
@@ -853,8 +877,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         return ldexpf(1.f, k);
       };
       uint32_t rr = 0, sgp = 0;  // bf16: ring index of the next stage, parities of the score slots
-      // bf16: the two halves of a row meet per page to agree on the page's
-      // maximum (and at a segment's end to add their row sums); bounded waits
+      uint32_t fph = 0;          // bf16, rows 32..63: parity of the forwarding barriers' next use
+      // bf16: the two halves of a row meet at a segment's end to add their
+      // row sums; bounded waits
       float* const xchg = reinterpret_cast<float*>(smem + kOffXchg);
       uint32_t xph = 0;
       auto exchange = [&](float v, float& other) -> bool {
@@ -879,7 +904,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         if (kFp8) {
           qmul = q_loaded ? qmul_next : load_q_f16(s);
         } else {
-          if (!q_loaded && !load_q_ring(rr)) { ok = false; break; }
+          if (!xq && !q_loaded && !load_q_ring(rr)) { ok = false; break; }
           rr += 2;  // the Q block's two stages
           qmul = 1.f;
         }
@@ -905,7 +930,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
               }
           }
           float x[kSC];
-          if (kFp8) {
+          float mt_page = 0.f;  // bf16: the page maximum over the row's 64 keys, scaled
+          if constexpr (kFp8) {
             // S = sum_g scale[token][g] * S_g, in fp32 from the group-score ring;
             // the tokens' scales are in the scale slot of the tile's stage
             const int stg = static_cast<int>(t % kStages);
@@ -952,34 +978,85 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kSC; ++i) x[i] = i < nv ? x[i] * row_scale : -INFINITY;
           } else {
-            const uint32_t slot = rr % kStages, sph3 = (sgp >> slot) & 1u;  // the page's stage and its use
-            sgp ^= 1u << slot;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
-              ok = false;
-              break;
+            // Both threads of a row read all 64 scores of the page: each takes
+            // the page maximum over all of them (so the two agree on it without
+            // exchanging anything) and exponentiates its own half (v0).
+            uint32_t v0[32], v1[32];
+            float4* const fwd_row = reinterpret_cast<float4*>(smem + kOffFwd) + hh * 256 + lane;
+            if (xq) {
+              // rows 32..63: the scores forwarded by warps 5 and 9 (one half each)
+              const bool got = mbar_wait(smem_u32(&bars->fwd_full[0]), fph, abort_flag) &&
+                               mbar_wait(smem_u32(&bars->fwd_full[1]), fph, abort_flag);
+              if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+              }
+              const float4* const oth_row = reinterpret_cast<const float4*>(smem + kOffFwd) + (hh ^ 1) * 256 + lane;
+#pragma unroll
+              for (int k4 = 0; k4 < 8; ++k4) {
+                const float4 y = fwd_row[32 * k4], z = oth_row[32 * k4];
+                v0[4 * k4 + 0] = __float_as_uint(y.x);
+                v0[4 * k4 + 1] = __float_as_uint(y.y);
+                v0[4 * k4 + 2] = __float_as_uint(y.z);
+                v0[4 * k4 + 3] = __float_as_uint(y.w);
+                v1[4 * k4 + 0] = __float_as_uint(z.x);
+                v1[4 * k4 + 1] = __float_as_uint(z.y);
+                v1[4 * k4 + 2] = __float_as_uint(z.z);
+                v1[4 * k4 + 3] = __float_as_uint(z.w);
+              }
+              mbar_arrive(smem_u32(&bars->fwd_empty[0]));
+              mbar_arrive(smem_u32(&bars->fwd_empty[1]));
+              fph ^= 1u;
+            } else {
+              const uint32_t slot = rr % kStages, sph3 = (sgp >> slot) & 1u;  // the page's stage and its use
+              sgp ^= 1u << slot;
+              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              tmem_ld32(tbase + lane_off + kColG + 64 * slot + c0, v0);         // this half's 32 keys
+              if (!fwd) tmem_ld32(tbase + lane_off + kColG + 64 * slot + (c0 ^ 32), v1);  // the other half's
+              tmem_wait_ld();
+              tc_fence_before();
+              mbar_arrive(smem_u32(&bars->sg_free[slot]));
+              if (fwd) {
+                // rows 32..63: hand the scores on (the previous page's were read)
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fwd_empty[hh]), fph ^ 1u, abort_flag))) {
+                  ok = false;
+                  break;
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4)
+                  fwd_row[32 * k4] = make_float4(__uint_as_float(v0[4 * k4 + 0]), __uint_as_float(v0[4 * k4 + 1]),
+                                                 __uint_as_float(v0[4 * k4 + 2]), __uint_as_float(v0[4 * k4 + 3]));
+                mbar_arrive(smem_u32(&bars->fwd_full[hh]));
+                fph ^= 1u;
+                continue;
+              }
             }
-            tc_fence_after();
-            uint32_t v0[32];
-            tmem_ld32(tbase + lane_off + kColG + 64 * slot + c0, v0);  // this half's 32 keys
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars->sg_free[slot]));
             // raw scores (the scale is applied in the exponent's FMA below);
             // keys the row does not see (only on a request's last pages) -> -inf
-            const int nv = n_vis - j * kPage - c0;  // keys of this half visible to the row
+            const int nv = n_vis - j * kPage - c0;         // keys of this half visible to the row
+            const int nvo = n_vis - j * kPage - (c0 ^ 32);  // ... of the other half
+            float xo[32];
 #pragma unroll
-            for (int i = 0; i < kSC; ++i) x[i] = __uint_as_float(v0[i]);
-            if (__any_sync(0xffffffffu, nv < kSC)) {
-#pragma unroll
-              for (int i = 0; i < kSC; ++i) x[i] = i < nv ? x[i] : -INFINITY;
+            for (int i = 0; i < 32; ++i) {
+              x[i] = __uint_as_float(v0[i]);
+              xo[i] = __uint_as_float(v1[i]);
             }
+            if (__any_sync(0xffffffffu, nv < 32 || nvo < 32)) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                x[i] = i < nv ? x[i] : -INFINITY;
+                xo[i] = i < nvo ? xo[i] : -INFINITY;
+              }
+            }
+            // the page's maximum over the whole row (the same value in both
+            // threads: max is exact), then scaled (softmax_scale > 0 commutes with it)
+            mt_page = fmaxf(max_n(x), max_n(xo)) * row_scale;
           }
-          float mt = max_n(x);
-          if (!kFp8) {  // the page's maximum over both halves of the row, then scaled
-            float other;
-            if (!exchange(mt, other)) { ok = false; break; }
-            mt = fmaxf(mt, other) * row_scale;  // softmax_scale > 0: the maximum commutes with it
-          }
+          float mt = kFp8 ? max_n(x) : mt_page;
           const float xs = kFp8 ? 1.f : row_scale;  // fp8: x is already scaled
           float alpha = 1.f;
           if (mt > m_ref + kRescaleLog2) {
@@ -1023,12 +1100,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
         if (!ok) break;
 
-        if (!kFp8) {  // the row sum over both halves
+        if (!kFp8 && !fwd) {  // the row sum over both halves
           float other;
           if (!exchange(l, other)) { ok = false; break; }
           l += other;
         }
-        if (hh == 0) {
+        if (hh == 0 && !fwd) {
           // the row sum and lse go to the accumulator, which writes the outputs
           const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
           if (!mbar_wait(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
@@ -1038,7 +1115,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         // Q of the next segment with pages can go in now: the QK of this
         // segment's last page is done (its scores were read), and the next
         // QK overlaps the accumulator's last PV and epilogue of this one
-        {
+        if (!xq) {
           SegIter look = it;
           Seg nx;
           while (look.next(nx)) {
