@@ -32,11 +32,14 @@
 //   warp 1 allocates TMEM and issues the MMAs from one lane; warps 2-5 (one
 //   TMEM lane quarter each, one query row per thread) run the softmax
 //   (scorer) or the rescale and epilogue (accumulator).  The bf16 scorer
-//   splits each row's softmax with warps 6-9 (keys 32..63 of a page).  The
-//   accumulator's PV commit multicasts the P-buffer credit straight to the
-//   scorer's barrier.  The fp8-cache variant has the loader bulk-copy each
-//   page's e4m3 bytes into the top of its ring stage, and warps 6-9 of both
-//   CTAs rewrite the stage in place as fp16 (the MMAs then run in fp16).
+//   splits each row's softmax with warps 6-9 (keys 32..63 of a page), and
+//   keeps arithmetic out of the MMA warp's SM sub-partition: warps 5 and 9
+//   only copy rows 32..63's scores to shared memory, where warps 10 and 11
+//   run their softmax.  The accumulator's PV commit multicasts the P-buffer
+//   credit straight to the scorer's barrier.  The fp8-cache variant has the
+//   loader bulk-copy each page's e4m3 bytes into the top of its ring stage,
+//   and warps 6, 7, 8 and 10 (variant B: 9) of both CTAs rewrite the stage in
+//   place as fp16 (the MMAs then run in fp16).
 // * Online softmax in base 2 with a lazy rescale: the running max only moves
 //   (and O is only rescaled) when a tile's max exceeds it by more than 8 (a
 //   factor 256); the final division by the row sum is exact either way.  This
@@ -145,13 +148,18 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Warps: loader, MMA issuer, four row warps (softmax of the scorer, rescale +
-// epilogue of the accumulator), then four more: the fp8 dequantisation, or
-// (bf16 scorer) the second half of each row's softmax.  The bf16 variant has
-// two more (warps 10 and 11), which run the softmax of rows 32..63 for the
-// scorer (below); they are idle in the accumulator.
-template <bool kFp8>
+// epilogue of the accumulator), then more:
+// - bf16: warps 6-9, the second half of each row's softmax (scorer), and
+//   warps 10 and 11, which run the softmax of rows 32..63 (below);
+// - fp8: the dequantisation on warps 6, 7, 8 and one more.  For variant A
+//   that is warp 10: warp 9 would share the MMA warp's SM sub-partition
+//   (warp % 4 == 1), where arithmetic slows every MMA issue 2-4x, so it stays
+//   idle (12% faster).  Variant B (heavier conversion: bf16 RoPE, scales read
+//   from the token records) measured 12-20% slower with warp 10 and with an
+//   idle eleventh warp than with ten warps and warp 9, so it keeps those.
+template <bool kFp8, bool kRopeB = false>
 struct Cfg {
-  static constexpr int kThreads = kFp8 ? 320 : 384;
+  static constexpr int kThreads = !kFp8 ? 384 : (kRopeB ? 320 : 352);
   static constexpr int kSoftmaxCols = kFp8 ? 64 : 32;  // keys of a page one softmax thread scores
 };
 
@@ -358,7 +366,7 @@ __device__ __forceinline__ float max_n(const float (&x)[n]) {
 // kRopeB (with kFp8): fp8 variant B, 656-byte token records (scales inside,
 // RoPE in bf16).
 template <bool kFp8, bool kRopeB = false>
-__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map_s, const __grid_constant__ CUtensorMap kv_map_a,
                       const __grid_constant__ CUtensorMap kv_map_r,
                       const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap out_map,
@@ -1431,8 +1439,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     if (!ok && !*abort_flag) signal_abort(bars, a.err, peer);
     if (!scorer && lane == 0) bulk_wait_all();  // output stores complete before the CTA ends
-  } else if (kFp8) {
-    // ---------------------------------------------------------------- fp8 dequant (warps 6-9)
+  } else if (kFp8 && (kRopeB || warp != 9)) {
+    // ---------------------------------------------------------------- fp8 dequant (warps 6-8, and 10 or 9)
     // This CTA's raw e4m3 chunks (64-byte swizzled, in the top of its stage)
     // -> fp16 blocks of the same stage, 128-byte swizzled as the MMA
     // descriptors expect.  The scorer writes the exact codes of its 9 blocks
@@ -1443,7 +1451,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     // blocks overwrite the raw chunks in place), then it converts and writes.
     // Rows past seqlen and pages with a bad id (read as zeros by TMA) are
     // written as zeros, with scale 0.
-    const int dq = tid - 192;                       // 0..127
+    const int dq = kRopeB ? tid - 192 : (warp == 10 ? 3 : warp - 6) * 32 + lane;  // 0..127
     const int t = dq & 63, h = dq >> 6;
     constexpr int kPieces = 18;                     // 16-channel pieces per thread (the scorer's count)
     const int n = scorer ? 18 : 16;                 // scorer: 36 pieces per token; accumulator: 32
@@ -1611,11 +1619,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
 int decode_smem_bytes(bool) { return kSmem; }
 
-static cudaLaunchConfig_t make_cfg(bool fp8, int clusters, cudaStream_t stream, cudaLaunchAttribute* attr,
+static cudaLaunchConfig_t make_cfg(bool fp8, bool rope_b, int clusters, cudaStream_t stream, cudaLaunchAttribute* attr,
                                    bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(fp8 ? Cfg<true>::kThreads : Cfg<false>::kThreads, 1, 1);
+  cfg.blockDim = dim3(!fp8 ? Cfg<false>::kThreads : (rope_b ? Cfg<true, true>::kThreads : Cfg<true, false>::kThreads), 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1644,8 +1652,8 @@ cudaError_t decode_max_active_clusters(bool fp8, int* clusters) {
   cudaError_t e = set_smem_attr(fp8);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_cfg(fp8, 1, nullptr, attr);
-  // both fp8 variants have the same block size and shared memory
+  cudaLaunchConfig_t cfg = make_cfg(fp8, false, 1, nullptr, attr);
+  // both fp8 variants have the same shared memory (one CTA per SM)
   if (fp8) return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<true, false>, &cfg);
   return cudaOccupancyMaxActiveClusters(clusters, mla_decode_kernel<false>, &cfg);
 }
@@ -1656,7 +1664,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kv_map_s, cons
   cudaError_t e = set_smem_attr(fp8);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_cfg(fp8, clusters, stream, attr, true);
+  cudaLaunchConfig_t cfg = make_cfg(fp8, fp8 && a.rope_bf16, clusters, stream, attr, true);
   if (fp8 && a.rope_bf16)
     return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, true>, kv_map_s, kv_map_a, kv_map_r, q_map, out_map,
                               out_map4, a);
