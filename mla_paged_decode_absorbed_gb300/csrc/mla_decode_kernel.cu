@@ -953,30 +953,32 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
                 ok = false;
                 break;
               }
-              tc_fence_after();
-              uint32_t v0[32], v1[32];
-              const uint32_t col = tbase + lane_off + kColG + 64 * slot;
-              tmem_ld32(col, v0);
-              tmem_ld32(col + 32, v1);
-              tmem_wait_ld();
-              tc_fence_before();
-              mbar_arrive(smem_u32(&bars->sg_free[slot]));
               // the dequant threads wrote the scales before completing the stage
               if (g == 0 &&
                   !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[stg]), (t / kStages) & 1u, abort_flag))) {
                 ok = false;
                 break;
               }
+              tc_fence_after();
+              const uint32_t col = tbase + lane_off + kColG + 64 * slot;
               const float4* sc4 = reinterpret_cast<const float4*>(scl + g * 64);
+              // the group's 64 scores in two halves of 32 (fewer live registers)
 #pragma unroll
-              for (int i4 = 0; i4 < kSC / 8; ++i4) {
-                const float4 a = sc4[i4], b = sc4[kSC / 8 + i4];
-                float* xa = x + 4 * i4;
-                float* xb = x + kSC / 2 + 4 * i4;
-                ffma2(xa[0], xa[1], __uint_as_float(v0[4 * i4 + 0]), __uint_as_float(v0[4 * i4 + 1]), a.x, a.y, xa[0], xa[1]);
-                ffma2(xa[2], xa[3], __uint_as_float(v0[4 * i4 + 2]), __uint_as_float(v0[4 * i4 + 3]), a.z, a.w, xa[2], xa[3]);
-                ffma2(xb[0], xb[1], __uint_as_float(v1[4 * i4 + 0]), __uint_as_float(v1[4 * i4 + 1]), b.x, b.y, xb[0], xb[1]);
-                ffma2(xb[2], xb[3], __uint_as_float(v1[4 * i4 + 2]), __uint_as_float(v1[4 * i4 + 3]), b.z, b.w, xb[2], xb[3]);
+              for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v0[32];
+                tmem_ld32(col + 32 * hf, v0);
+                tmem_wait_ld();
+                if (hf == 1) {
+                  tc_fence_before();
+                  mbar_arrive(smem_u32(&bars->sg_free[slot]));
+                }
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4) {
+                  const float4 sc = sc4[8 * hf + i4];
+                  float* xa = x + 32 * hf + 4 * i4;
+                  ffma2(xa[0], xa[1], __uint_as_float(v0[4 * i4 + 0]), __uint_as_float(v0[4 * i4 + 1]), sc.x, sc.y, xa[0], xa[1]);
+                  ffma2(xa[2], xa[3], __uint_as_float(v0[4 * i4 + 2]), __uint_as_float(v0[4 * i4 + 3]), sc.z, sc.w, xa[2], xa[3]);
+                }
               }
             }
             if (!ok) break;
