@@ -35,10 +35,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kCombineChunksPerCta = 4;  // 8-channel chunks of every row per combine CTA
-constexpr int kCombineThreads = 128 * kCombineChunksPerCta;
-constexpr int kCombineJobColumns = 4;     // CTA columns of the combine grid (they stride over jobs)
-constexpr int kCombineBatch = 16;        // partial pieces whose loads a combine thread keeps in flight
+constexpr int kCombineSplit = 4;          // threads per (row, chunk): each merges every 4th piece
+constexpr int kCombineThreads = 128 * kCombineSplit;
+constexpr int kCombineBatch = 8;         // partial pieces whose loads a combine thread keeps in flight
 
 // ------------------------------------------------------------------ planner
 // Cost of unit u (row block rb = u / B of request b = u % B): the pages the
@@ -183,23 +182,24 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
 }
 
 // ------------------------------------------------------------------ combine
-// One combine job, one 8-channel chunk `j` of row L of the unit's row block.
-__device__ __forceinline__ void combine_rows(const CombineArgs& a, const float2* lp, const uint4* op, int4 job,
-                                             int L, int j) {
-  const int u = job.x, c = job.y, last = job.z, slot0 = job.w;
-  const int b = u % a.B, rb = u / a.B;
-  const int r = rb * kRowsPerBlock + L;
-  if (r >= a.R) return;
-  // pieces in batches of kCombineBatch (all loads of a batch issued together), with a
-  // running max across batches
-  float mx = -INFINITY, wsum = 0.f;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int cb = c; cb <= last; cb += kCombineBatch) {
+// Part q of one combine job's merge for 8-channel chunk j of row L of the
+// unit's row block: pieces c + q, c + q + kCombineSplit, ... in batches of
+// kCombineBatch (all loads of a batch issued together), with a running
+// maximum: returns (max lse, sum of exp(lse_k - max), sum of
+// exp(lse_k - max) * out_k over 8 channels), out_k = stored_k * scale_k.
+__device__ __forceinline__ void combine_part(const float2* lp, const uint4* op, int4 job, int L, int j, int q,
+                                             float& mx, float& wsum, float (&acc)[8]) {
+  const int c = job.y, last = job.z, slot0 = job.w;
+  mx = -INFINITY;
+  wsum = 0.f;
+#pragma unroll
+  for (int h = 0; h < 8; ++h) acc[h] = 0.f;
+  for (int cb = c + q; cb <= last; cb += kCombineSplit * kCombineBatch) {
     float2 ls[kCombineBatch];
     uint4 o[kCombineBatch];
 #pragma unroll
     for (int i = 0; i < kCombineBatch; ++i) {
-      const int cc = cb + i;
+      const int cc = cb + kCombineSplit * i;
       ls[i] = make_float2(-INFINITY, 0.f);
       o[i] = make_uint4(0, 0, 0, 0);
       if (cc <= last) {
@@ -232,39 +232,76 @@ __device__ __forceinline__ void combine_rows(const CombineArgs& a, const float2*
     }
     mx = m_new;
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const size_t orow = static_cast<size_t>(b) * a.R + r;
-  uint32_t packed[4];
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * h] * inv, acc[2 * h + 1] * inv);
-    packed[h] = *reinterpret_cast<uint32_t*>(&v);
-  }
-  reinterpret_cast<uint4*>(a.out + orow * kDv)[j] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  if (j == 0) a.lse[orow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 // Units with at most kFuseMax pieces are merged inside the attention kernel;
 // this kernel merges the others (the planner's job list: unit, first and last
-// cluster, slot of the first piece).  CTA (x, y) takes jobs x, x + gridDim.x,
-// ... and 8-channel chunks [4y, 4y + 4) of every row, one row per thread, so
-// the chunk-interleaved fp16 partial slots are read with coalesced loads:
-//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k,
-// where out_k = stored_k * scale_k.  Pieces go in batches of 8 whose loads
-// are all issued together, with a running maximum across batches.
+// cluster, slot of the first piece), job after job.  CTA (x, y) takes the
+// 8-channel chunk j = y * gridDim.x + x of every row (gridDim.x * gridDim.y =
+// 64 chunks, so a single job already keeps 64 SMs busy); thread (q, L) takes
+// row L and every kCombineSplit-th piece from q, so the chunk-interleaved
+// fp16 partial slots are read with coalesced loads.  The kCombineSplit part
+// merges meet in shared memory, and thread (0, L) finishes the row:
+//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) * out_k.
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineArgs a) {
+  __shared__ float s_m[kCombineSplit][kRowsPerBlock], s_w[kCombineSplit][kRowsPerBlock];
+  __shared__ float s_acc[kCombineSplit][8][kRowsPerBlock];
   // launched as a programmatic dependent of the attention kernel: wait for it
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // CTA columns stride over the jobs; the planner packs them in front of the
-  // unused slots, which hold unit -1
-  const int L = threadIdx.x & (kRowsPerBlock - 1);                      // row within the block
-  const int j = blockIdx.y * kCombineChunksPerCta + (threadIdx.x >> 7);  // 8-channel chunk
+  const int L = threadIdx.x & (kRowsPerBlock - 1);  // row within the block
+  const int q = threadIdx.x >> 7;                   // which pieces
+  const int j = blockIdx.y * gridDim.x + blockIdx.x;  // 8-channel chunk
   const float2* lp = reinterpret_cast<const float2*>(a.lse_part);
   const uint4* op = reinterpret_cast<const uint4*>(a.o_part);
-  for (int jb = blockIdx.x; jb < a.clusters; jb += gridDim.x) {
-    const int4 job = reinterpret_cast<const int4*>(a.sync + 4 * a.clusters)[jb];
-    if (job.x < 0) return;
-    combine_rows(a, lp, op, job, L, j);
+  // the planner packs the jobs in front of the unused slots, which hold unit -1
+  const int4* jobs = reinterpret_cast<const int4*>(a.sync + 4 * a.clusters);
+  for (int jb = 0; jb < a.clusters; ++jb) {
+    const int4 job = jobs[jb];
+    if (job.x < 0) break;  // the same job for every thread of the CTA
+    const int b = job.x % a.B, rb = job.x / a.B;
+    const int r = rb * kRowsPerBlock + L;
+    float mx, wsum, acc[8];
+    if (r < a.R) {
+      combine_part(lp, op, job, L, j, q, mx, wsum, acc);
+    } else {
+      mx = -INFINITY;
+      wsum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[h] = 0.f;
+    }
+    s_m[q][L] = mx;
+    s_w[q][L] = wsum;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) s_acc[q][h][L] = acc[h];
+    __syncthreads();
+    if (q == 0 && r < a.R) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kCombineSplit; ++k) m = fmaxf(m, s_m[k][L]);
+      float w = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < kCombineSplit; ++k) {
+          const float mk = s_m[k][L];
+          if (mk == -INFINITY) continue;  // that part saw no key of this row
+          const float e = expf(mk - m);
+          w += e * s_w[k][L];
+#pragma unroll
+          for (int h = 0; h < 8; ++h) o[h] += e * s_acc[k][h][L];
+        }
+      }
+      const float inv = w > 0.f ? 1.f / w : 0.f;
+      const size_t orow = static_cast<size_t>(b) * a.R + r;
+      uint32_t packed[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(o[2 * h] * inv, o[2 * h + 1] * inv);
+        packed[h] = *reinterpret_cast<uint32_t*>(&v);
+      }
+      reinterpret_cast<uint4*>(a.out + orow * kDv)[j] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      if (j == 0) a.lse[orow] = w > 0.f ? m + logf(w) : -INFINITY;
+    }
+    __syncthreads();  // the shared arrays are rewritten by the next job
   }
 }
 
@@ -683,12 +720,10 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   a.overhead = p.x.ovh;
   // programmatic dependent of the attention kernel (it waits on the device)
   cudaLaunchConfig_t cfg = {};
-  // a job unit has more than kFuseMax pieces, so it spans at least kFuseMax of
-  // the G - 1 cluster boundaries: there are at most (G - 1) / kFuseMax jobs.
-  // A few CTA columns stride over them: a grid sized for the worst case cost
-  // several microseconds per step to schedule even when there is no job.
-  const int max_jobs = p.G > kFuseMax ? (p.G - 1) / kFuseMax : 1;
-  cfg.gridDim = dim3(max_jobs < kCombineJobColumns ? max_jobs : kCombineJobColumns, kPartChunks / kCombineChunksPerCta, 1);
+  // one CTA per 8-channel chunk, looping over the jobs: a grid sized for the
+  // worst-case job count cost several microseconds per step to schedule even
+  // when there is no job
+  cfg.gridDim = dim3(4, kPartChunks / 4, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
