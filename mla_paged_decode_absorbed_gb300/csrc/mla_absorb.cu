@@ -34,7 +34,7 @@ namespace {
 
 using namespace mla_sm103;
 
-constexpr int kGemmThreads = 128;           // warp 0 loads, warp 1 issues MMAs, all four run the epilogue
+constexpr int kGemmThreads = 128;           // thread 0 loads, warp 1 issues MMAs, all four run the epilogue
 constexpr int kChunkA = 128 * 64 * 2;       // one 64-channel chunk of a 128-row A tile (16 KB)
 constexpr int kNopeDim = 128, kRopeDim = 64, kLat = 512;
 
@@ -79,6 +79,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(smem_u32(&full[1]), 1);
     mbar_init(smem_u32(done), 1);
     fence_mbarrier_init_cluster();
+    // ------------------------------------------------------------ loads
+    // issued at once (the barriers are this thread's own), so their latency
+    // overlaps the TMEM allocation and the block barrier below
+    tma_prefetch_desc(&map_w);
+    tma_prefetch_desc(&map_x);
+    uint8_t* const sa0 = smem;
+    uint8_t* const sb0 = smem + kA;
+    const uint32_t f0 = smem_u32(&full[0]), f1 = smem_u32(&full[1]);
+    if (kProject) {
+      // B: every 64-channel chunk of the tile's tokens (chunk-major), and the
+      // first 256 k rows of W_UV[h] (both 64-wide output-channel halves);
+      // then the other 256 rows on their own barrier
+      mbar_arrive_expect_tx(f0, static_cast<uint32_t>(b_bytes + kA / 2));
+      tma_load_4d(smem_u32(sb0), &map_x, 0, t0, 0, h, f0);
+      tma_load_3d(smem_u32(sa0), &map_w, 0, h * kLat, 0, f0);
+      mbar_arrive_expect_tx(f1, static_cast<uint32_t>(kA / 2));
+      tma_load_3d(smem_u32(sa0 + kA / 2), &map_w, 0, h * kLat + 256, 0, f1);
+    } else {
+      // W_UK[h] rows n = 128x.. (both 64-channel chunks) and the tokens' q_nope
+      mbar_arrive_expect_tx(f0, static_cast<uint32_t>(kA + b_bytes));
+      tma_load_3d(smem_u32(sa0), &map_w, 0, h * kLat + 128 * xt, 0, f0);
+      tma_load_4d(smem_u32(sb0), &map_x, 0, t0, 0, h, f0);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(tt));
@@ -91,28 +114,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* const sa = smem;
   uint8_t* const sb = smem + kA;
 
-  bool ok = true;
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ loader
-    tma_prefetch_desc(&map_w);
-    tma_prefetch_desc(&map_x);
-    const uint32_t f0 = smem_u32(&full[0]), f1 = smem_u32(&full[1]);
-    if (kProject) {
-      // B: every 64-channel chunk of the tile's tokens (chunk-major), and the
-      // first 256 k rows of W_UV[h] (both 64-wide output-channel halves);
-      // then the other 256 rows on their own barrier
-      mbar_arrive_expect_tx(f0, static_cast<uint32_t>(b_bytes + kA / 2));
-      tma_load_4d(smem_u32(sb), &map_x, 0, t0, 0, h, f0);
-      tma_load_3d(smem_u32(sa), &map_w, 0, h * kLat, 0, f0);
-      mbar_arrive_expect_tx(f1, static_cast<uint32_t>(kA / 2));
-      tma_load_3d(smem_u32(sa + kA / 2), &map_w, 0, h * kLat + 256, 0, f1);
-    } else {
-      // W_UK[h] rows n = 128x.. (both 64-channel chunks) and the tokens' q_nope
-      mbar_arrive_expect_tx(f0, static_cast<uint32_t>(kA + b_bytes));
-      tma_load_3d(smem_u32(sa), &map_w, 0, h * kLat + 128 * xt, 0, f0);
-      tma_load_4d(smem_u32(sb), &map_x, 0, t0, 0, h, f0);
+  // absorb: the RoPE part of q passes through, q[t, h, 512:576] = q_rope[t, h].
+  // The four CTAs of a token tile (x = 0..3) copy a quarter of its tokens each,
+  // and the loads are issued now, so that their latency overlaps the operand
+  // loads instead of lengthening one CTA's epilogue (tt / 4 tokens x 8
+  // 16-byte pieces = 2 tt pieces per CTA, at most four per thread)
+  uint4 rope_v[4];
+  if (!kProject) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + i * kGemmThreads, t = t0 + xt * (tt / 4) + (idx >> 3);
+      rope_v[i] = make_uint4(0, 0, 0, 0);
+      if (idx < 2 * tt && t < a.T)
+        rope_v[i] = __ldg(reinterpret_cast<const uint4*>(a.rope + (static_cast<size_t>(t) * a.H + h) * kRopeDim) + (idx & 7));
     }
-  } else if (warp == 1 && lane == 0) {
+  }
+
+  bool ok = true;
+  if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, tt, kProject, false);
     // B: K-major token rows, chunk c at c * tt * 128 bytes
@@ -179,15 +198,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *reinterpret_cast<uint4*>(dst) = reinterpret_cast<const uint4*>(stg + row * 128)[q16];
       }
     }
-    if (!kProject && xt == 0) {
-      // the RoPE part of q passes through: q[t, h, 512:576] = q_rope[t, h]
-      for (int idx = tid; idx < tt * 8; idx += kGemmThreads) {
-        const int row = idx >> 3, q8 = idx & 7, t = t0 + row;
-        if (t < a.T) {
-          const size_t th = static_cast<size_t>(t) * a.H + h;
-          reinterpret_cast<uint4*>(a.y + th * kDqk + kLat)[q8] =
-              reinterpret_cast<const uint4*>(a.rope + th * kRopeDim)[q8];
-        }
+    if (!kProject) {  // this CTA's quarter of the tile's RoPE pieces, loaded at the start
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = tid + i * kGemmThreads, t = t0 + xt * (tt / 4) + (idx >> 3);
+        if (idx < 2 * tt && t < a.T)
+          reinterpret_cast<uint4*>(a.y + (static_cast<size_t>(t) * a.H + h) * kDqk + kLat)[idx & 7] = rope_v[i];
       }
     }
   }
