@@ -38,6 +38,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kCombineSplit = 4;          // threads per (row, chunk): each merges every 4th piece
 constexpr int kCombineThreads = 128 * kCombineSplit;
 constexpr int kCombineBatch = 8;         // partial pieces whose loads a combine thread keeps in flight
+constexpr int kCombineJobColumns = 3;    // CTA columns of the combine grid; column x takes jobs x, x + 3, ...
 
 // ------------------------------------------------------------------ planner
 // Cost of unit u (row block rb = u / B of request b = u % B): the pages the
@@ -236,9 +237,10 @@ __device__ __forceinline__ void combine_part(const float2* lp, const uint4* op, 
 
 // Units with at most kFuseMax pieces are merged inside the attention kernel;
 // this kernel merges the others (the planner's job list: unit, first and last
-// cluster, slot of the first piece), job after job.  CTA (x, y) takes the
-// 8-channel chunk j = y * gridDim.x + x of every row (gridDim.x * gridDim.y =
-// 64 chunks, so a single job already keeps 64 SMs busy); thread (q, L) takes
+// cluster, slot of the first piece).  CTA (j, x) takes the 8-channel chunk j
+// of every row (64 chunks, so a single job already keeps 64 SMs busy) of jobs
+// x, x + kCombineJobColumns, ... (the jobs' rounds of dependent loads then
+// overlap instead of adding up); thread (q, L) takes
 // row L and every kCombineSplit-th piece from q, so the chunk-interleaved
 // fp16 partial slots are read with coalesced loads.  The kCombineSplit part
 // merges meet in shared memory, and thread (0, L) finishes the row:
@@ -250,12 +252,12 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int L = threadIdx.x & (kRowsPerBlock - 1);  // row within the block
   const int q = threadIdx.x >> 7;                   // which pieces
-  const int j = blockIdx.y * gridDim.x + blockIdx.x;  // 8-channel chunk
+  const int j = blockIdx.x;                         // 8-channel chunk
   const float2* lp = reinterpret_cast<const float2*>(a.lse_part);
   const uint4* op = reinterpret_cast<const uint4*>(a.o_part);
   // the planner packs the jobs in front of the unused slots, which hold unit -1
   const int4* jobs = reinterpret_cast<const int4*>(a.sync + 4 * a.clusters);
-  for (int jb = 0; jb < a.clusters; ++jb) {
+  for (int jb = blockIdx.y; jb < a.clusters; jb += gridDim.y) {
     const int4 job = jobs[jb];
     if (job.x < 0) break;  // the same job for every thread of the CTA
     const int b = job.x % a.B, rb = job.x / a.B;
@@ -720,10 +722,10 @@ mla_status run_combine(const Prepared& p, void* out, float* lse, cudaStream_t st
   a.overhead = p.x.ovh;
   // programmatic dependent of the attention kernel (it waits on the device)
   cudaLaunchConfig_t cfg = {};
-  // one CTA per 8-channel chunk, looping over the jobs: a grid sized for the
-  // worst-case job count cost several microseconds per step to schedule even
-  // when there is no job
-  cfg.gridDim = dim3(4, kPartChunks / 4, 1);
+  // one CTA per 8-channel chunk and job column, each column looping over its
+  // jobs: a grid sized for the worst-case job count cost several microseconds
+  // per step to schedule even when there is no job
+  cfg.gridDim = dim3(kPartChunks, kCombineJobColumns, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
