@@ -363,6 +363,19 @@ __device__ __forceinline__ float max_n(const float (&x)[n]) {
   return fmax3(m0, m1, fmax3(x[n - 2], x[n - 1], x[n - 2]));
 }
 
+// Bounded barrier wait, its waiting loop inlined or out of line (kOut).  The
+// fp8 variant A kernel ran 9% faster with the loops out of line (less code for
+// its warps to fetch); the bf16 kernel ran 6% slower on the MTP workload that
+// way, and variant B was not measured, so both keep them inline.
+template <bool kOut, bool kClusterAcquire = false>
+__device__ __forceinline__ bool kwait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  if constexpr (kOut) {
+    return mbar_wait_ool<kClusterAcquire>(bar, parity, abort_flag);
+  } else {
+    return mbar_wait<kClusterAcquire>(bar, parity, abort_flag);
+  }
+}
+
 // kRopeB (with kFp8): fp8 variant B, 656-byte token records (scales inside,
 // RoPE in bf16).
 template <bool kFp8, bool kRopeB = false>
@@ -371,6 +384,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
                       const __grid_constant__ CUtensorMap kv_map_r,
                       const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap out_map,
                       const __grid_constant__ CUtensorMap out_map4, const DecodeArgs a) {
+  constexpr bool kOutWait = kFp8 && !kRopeB;  // see kwait
   constexpr int kStagesA = AccLayout<kFp8>::kStagesA, kPBufs = AccLayout<kFp8>::kPBufs;
   constexpr int kOffP = AccLayout<kFp8>::kOffP, kOffAlpha = AccLayout<kFp8>::kOffAlpha, kOffL = AccLayout<kFp8>::kOffL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -499,7 +513,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       if (s.empty) continue;
       for (int h = 0; q_ring && h < 2; ++h) {
         if (lane == 0) {
-          if (!mbar_wait(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
+          if (!kwait<kOutWait>(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
             ok = false;
             if (!*abort_flag) signal_abort(bars, a.err, peer);
           } else {
@@ -526,13 +540,13 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
           int pid = __shfl_sync(0xffffffffu, my_pid, k);
           if (lane == 0 && wait_first_p) {
             wait_first_p = false;
-            if (!mbar_wait<true>(smem_u32(&bars->p_full[0]), 0u, abort_flag)) {
+            if (!kwait<kOutWait, true>(smem_u32(&bars->p_full[0]), 0u, abort_flag)) {
               ok = false;
               if (!*abort_flag) signal_abort(bars, a.err, peer);
             }
           }
           if (lane == 0 && ok) {
-            if (!mbar_wait(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
+            if (!kwait<kOutWait>(smem_u32(&bars->kv_empty[stage]), ph ^ 1u, abort_flag)) {
               ok = false;
               if (!*abort_flag) signal_abort(bars, a.err, peer);
             } else {
@@ -579,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       // wait (time-bounded only) for the loads already in flight
       for (int i = 0; i < nst; ++i)
         if (last_par[i] >= 0)
-          mbar_wait(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
+          kwait<kOutWait>(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -593,7 +607,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
     if (scorer && __ldg(a.hdr + kHdrStall) != 0) {
       // a test's stall request: wait on a barrier nothing signals, so the
       // bounded wait runs out and the whole cluster takes its abort path
-      if (!mbar_wait(smem_u32(&bars->stall), 0u, abort_flag)) ok = false;
+      if (!kwait<kOutWait>(smem_u32(&bars->stall), 0u, abort_flag)) ok = false;
     }
     if (scorer) {
       // S = Q K^T: 36 steps of K=16 over the 576 channels, A = Q in TMEM.
@@ -614,7 +628,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       uint32_t sgp = 0;
       while (ok && it.next(s)) {
         if (s.empty) continue;
-        if (!mbar_wait(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
+        if (!kwait<kOutWait>(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
         q_ph ^= 1u;
         if (!kFp8) {
           // Q is in TMEM, so the two stages that brought it are free
@@ -627,13 +641,13 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
           }
         }
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
-          if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutWait>(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
           const uint64_t b0 = smem_desc_sw128(smem_u32(smem + stage * kStageS), 16, kFp8 ? 1024 : kTokGroupStride);
           if (kFp8) {
             for (int g = 0; g < kGroups && ok; ++g, ++gj) {
               const uint32_t slot = gj % kGroupSlots, gph = (gj / kGroupSlots) & 1u;
               // warp-uniform outcome: the issue below ends in __syncwarp
-              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_free[slot]), gph ^ 1u, abort_flag))) {
+              if (!__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->sg_free[slot]), gph ^ 1u, abort_flag))) {
                 ok = false;
                 break;
               }
@@ -654,10 +668,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
             // (not a segment's first page: the page after it goes to a stage the
             // segment's Q block frees only once Q is in TMEM)
             const bool pair = stage < kStages - 1 && j > s.page_lo && j + 1 < s.page_hi;
-            bool ready = mbar_wait(smem_u32(&bars->sg_free[stage]), ((sgp >> stage) & 1u) ^ 1u, abort_flag);
+            bool ready = kwait<kOutWait>(smem_u32(&bars->sg_free[stage]), ((sgp >> stage) & 1u) ^ 1u, abort_flag);
             if (pair) {
-              ready = ready && mbar_wait(smem_u32(&bars->kv_full[stage + 1]), ph, abort_flag) &&
-                      mbar_wait(smem_u32(&bars->sg_free[stage + 1]), ((sgp >> (stage + 1)) & 1u) ^ 1u, abort_flag);
+              ready = ready && kwait<kOutWait>(smem_u32(&bars->kv_full[stage + 1]), ph, abort_flag) &&
+                      kwait<kOutWait>(smem_u32(&bars->sg_free[stage + 1]), ((sgp >> (stage + 1)) & 1u) ^ 1u, abort_flag);
             }
             sgp ^= (pair ? 3u : 1u) << stage;
             if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }  // uniform: the issue ends in __syncwarp
@@ -706,16 +720,16 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         const int seqlen = clamp_seqlen(__ldg(a.seqlens + s.b), a.max_pages);
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t % kPBufs;
-          if (!mbar_wait(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutWait>(smem_u32(&bars->kv_full[stage]), ph, abort_flag)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageO;
           if (!kFp8) {
             const int valid = seqlen - j * kPage;
             if (valid < kPage) zero_tail_rows(st, valid > 0 ? valid : 0, 8, lane);
             __syncwarp();
           }
-          if (!mbar_wait(smem_u32(&bars->corr_done[sb]), (t / kPBufs) & 1u, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutWait>(smem_u32(&bars->corr_done[sb]), (t / kPBufs) & 1u, abort_flag)) { ok = false; break; }
           if (j == s.page_lo) {
-            if (!mbar_wait(smem_u32(&bars->o_free), ofree_ph ^ 1u, abort_flag)) { ok = false; break; }
+            if (!kwait<kOutWait>(smem_u32(&bars->o_free), ofree_ph ^ 1u, abort_flag)) { ok = false; break; }
             ofree_ph ^= 1u;
           }
           tc_fence_after();
@@ -748,7 +762,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
     if (!ok && !*abort_flag && lane == 0) signal_abort(bars, a.err, peer);
     if (lane == 0) {
       mma_commit(smem_u32(&bars->drain));
-      mbar_wait(smem_u32(&bars->drain), 0u, nullptr);
+      kwait<kOutWait>(smem_u32(&bars->drain), 0u, nullptr);
     }
     __syncwarp();
   } else if (warp < 6 || (!kFp8 && scorer)) {
@@ -794,7 +808,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       auto load_q_ring = [&](uint32_t r0) -> bool {
         const uint32_t rq = r0 + (L >= 64 ? 1u : 0u);
         const uint32_t st = rq % kStages;
-        if (!mbar_wait(smem_u32(&bars->kv_full[st]), (rq / kStages) & 1u, abort_flag)) return false;
+        if (!kwait<kOutWait>(smem_u32(&bars->kv_full[st]), (rq / kStages) & 1u, abort_flag)) return false;
         const uint8_t* qs_base = smem + st * kStageS;
         const int row = L & 63;
         for (int c = hh ? 5 : 0; c < (hh ? 9 : 5); ++c) {
@@ -902,7 +916,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       auto exchange = [&](float v, float& other) -> bool {
         xchg[((xph & 1u) * 2 + hh) * kRowsPerBlock + L] = v;
         mbar_arrive(smem_u32(&bars->mx_bar[wq]));
-        const bool done = mbar_wait(smem_u32(&bars->mx_bar[wq]), xph & 1u, abort_flag);
+        const bool done = kwait<kOutWait>(smem_u32(&bars->mx_bar[wq]), xph & 1u, abort_flag);
         other = xchg[((xph & 1u) * 2 + (hh ^ 1)) * kRowsPerBlock + L];
         ++xph;
         return done;
@@ -958,13 +972,13 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
             for (int g = 0; g < kGroups; ++g, ++gj) {
               const uint32_t slot = gj % kGroupSlots, gph = (gj / kGroupSlots) & 1u;
               // warp-uniform outcome: tcgen05.ld below is a warp-wide instruction
-              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), gph, abort_flag))) {
+              if (!__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->sg_full[slot]), gph, abort_flag))) {
                 ok = false;
                 break;
               }
               // the dequant threads wrote the scales before completing the stage
               if (g == 0 &&
-                  !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[stg]), (t / kStages) & 1u, abort_flag))) {
+                  !__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->kv_full[stg]), (t / kStages) & 1u, abort_flag))) {
                 ok = false;
                 break;
               }
@@ -1004,8 +1018,8 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
             float4* const fwd_row = reinterpret_cast<float4*>(smem + kOffFwd) + hh * 256 + lane;
             if (xq) {
               // rows 32..63: the scores forwarded by warps 5 and 9 (one half each)
-              const bool got = mbar_wait(smem_u32(&bars->fwd_full[0]), fph, abort_flag) &&
-                               mbar_wait(smem_u32(&bars->fwd_full[1]), fph, abort_flag);
+              const bool got = kwait<kOutWait>(smem_u32(&bars->fwd_full[0]), fph, abort_flag) &&
+                               kwait<kOutWait>(smem_u32(&bars->fwd_full[1]), fph, abort_flag);
               if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
@@ -1029,7 +1043,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
             } else {
               const uint32_t slot = rr % kStages, sph3 = (sgp >> slot) & 1u;  // the page's stage and its use
               sgp ^= 1u << slot;
-              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
+              if (!__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->sg_full[slot]), sph3, abort_flag))) {
                 ok = false;
                 break;
               }
@@ -1041,7 +1055,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
               mbar_arrive(smem_u32(&bars->sg_free[slot]));
               if (fwd) {
                 // rows 32..63: hand the scores on (the previous page's were read)
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fwd_empty[hh]), fph ^ 1u, abort_flag))) {
+                if (!__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->fwd_empty[hh]), fph ^ 1u, abort_flag))) {
                   ok = false;
                   break;
                 }
@@ -1108,7 +1122,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
 
           // this thread's part of P tile t (16-byte granules c0/8 ..) and, from
           // the first half, the row's factor to the accumulator (its buffer sb must be free)
-          if (!mbar_wait(smem_u32(&bars->pbuf_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutWait>(smem_u32(&bars->pbuf_free[sb]), sph ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t pbar = rPfull0 + 8u * sb;
           const uint32_t prow = rP + sb * kPBytes + L * 128;
 #pragma unroll
@@ -1127,7 +1141,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         if (hh == 0 && !fwd) {
           // the row sum and lse go to the accumulator, which writes the outputs
           const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
-          if (!mbar_wait(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutWait>(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           st_async_v2_f32(rL + L * 8, l, lse_v, rLfull);
           ++seg_n;
         }
@@ -1159,7 +1173,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       uint32_t ofull_ph = 0, epi_ph = 0, mrg_n = 0;
       auto epi_sync = [&]() -> bool {
         mbar_arrive(smem_u32(&bars->epi_bar));
-        const bool done = mbar_wait(smem_u32(&bars->epi_bar), epi_ph, abort_flag);
+        const bool done = kwait<kOutWait>(smem_u32(&bars->epi_bar), epi_ph, abort_flag);
         epi_ph ^= 1u;
         return done;
       };
@@ -1191,14 +1205,14 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         for (int j = s.page_lo; j < s.page_hi; ++j, ++t) {
           const uint32_t sb = t % kPBufs, sph = (t / kPBufs) & 1u;
           if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->p_full[sb]), kPBytes + kVecBytes);
-          if (!mbar_wait<true>(smem_u32(&bars->p_full[sb]), sph, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutWait, true>(smem_u32(&bars->p_full[sb]), sph, abort_flag)) { ok = false; break; }
           if (j + 1 == s.page_hi && s.split && split_k <= kFuseMax && ctid == 0)
             ticket = atomicAdd(a.unit_cnt + split_c0, 1);
           const float alpha = alpha_s[sb * kRowsPerBlock + L];
           if (__any_sync(0xffffffffu, alpha != 1.f) && j > s.page_lo) {
             // O must hold PV of the previous tile before it is rescaled
             const uint32_t pb = (t - 1u) % kPBufs, pph = ((t - 1u) / kPBufs) & 1u;
-            if (!mbar_wait(smem_u32(&bars->pv_done[pb]), pph, abort_flag)) { ok = false; break; }
+            if (!kwait<kOutWait>(smem_u32(&bars->pv_done[pb]), pph, abort_flag)) { ok = false; break; }
             tc_fence_after();
             for (int ch = 0; ch < 16; ++ch) {
               uint32_t o[32];
@@ -1223,10 +1237,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         //  2  the last piece to finish of a unit with at most kFuseMax pieces:
         //     merges the other pieces' partials with its own O (the LSE merge)
         //     and writes out and lse itself.
-        if (!mbar_wait(smem_u32(&bars->o_full), ofull_ph, abort_flag)) { ok = false; break; }
+        if (!kwait<kOutWait>(smem_u32(&bars->o_full), ofull_ph, abort_flag)) { ok = false; break; }
         ofull_ph ^= 1u;
         if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->l_full), kRowsPerBlock * 8);
-        if (!mbar_wait<true>(smem_u32(&bars->l_full), seg_n & 1u, abort_flag)) { ok = false; break; }
+        if (!kwait<kOutWait, true>(smem_u32(&bars->l_full), seg_n & 1u, abort_flag)) { ok = false; break; }
         const float2 lrow = l_s[L];  // (row sum, lse) of this piece
         ++seg_n;
         const float l = lrow.x, lse_own = lrow.y;
@@ -1369,7 +1383,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
                 for (int off = 0; off < kPartBytes; off += 32768)
                   bulk_load(smem_u32(smem + off), reinterpret_cast<const uint8_t*>(gsrc) + off, 32768, mb);
               }
-              if (!mbar_wait(smem_u32(&bars->mrg_bar), mrg_n & 1u, abort_flag)) { ok = false; break; }
+              if (!kwait<kOutWait>(smem_u32(&bars->mrg_bar), mrg_n & 1u, abort_flag)) { ok = false; break; }
               ++mrg_n;
               src = reinterpret_cast<const uint4*>(smem) + L;
             }
@@ -1505,7 +1519,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
           }
         }
         // warp-uniform outcomes (the page-id shuffle above is warp-wide)
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->raw_full[stage]), ph, abort_flag))) {
+        if (!__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->raw_full[stage]), ph, abort_flag))) {
           ok = false;
           break;
         }
@@ -1531,7 +1545,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         }
         // every thread has its raw pieces: the fp16 blocks may now overwrite them
         mbar_arrive(smem_u32(&bars->dq_sync));
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dq_sync), sync_ph, abort_flag))) {
+        if (!__all_sync(0xffffffffu, kwait<kOutWait>(smem_u32(&bars->dq_sync), sync_ph, abort_flag))) {
           ok = false;
           break;
         }

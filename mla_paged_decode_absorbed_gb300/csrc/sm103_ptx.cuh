@@ -106,6 +106,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same wait with its waiting loop out of line, for kernels with many wait
+// sites where the inlined loops enlarge the code the warps fetch.
+template <bool kClusterAcquire>
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (kClusterAcquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+      return true;
+    if ((it & 15u) == 0u) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) return false;
+    }
+  }
+}
+template <bool kClusterAcquire = false>
+__device__ __forceinline__ bool mbar_wait_ool(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  if (kClusterAcquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow<kClusterAcquire>(bar, parity, abort_flag);
+}
+
 // ------------------------------------------------------------- cluster / DSMEM
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank) {
   uint32_t r;
