@@ -364,9 +364,10 @@ __device__ __forceinline__ float max_n(const float (&x)[n]) {
 }
 
 // Bounded barrier wait, its waiting loop inlined or out of line (kOut).  The
-// fp8 variant A kernel ran 9% faster with the loops out of line (less code for
-// its warps to fetch); the bf16 kernel ran 6% slower on the MTP workload that
-// way, and variant B was not measured, so both keep them inline.
+// fp8 variant A kernel ran 9% faster with every loop out of line (less code
+// for its warps to fetch); the bf16 kernel ran 6% slower on the MTP workload
+// that way, so it keeps the loops of its per-page waits inline; variant B was
+// not measured and keeps all of them inline.
 template <bool kOut, bool kClusterAcquire = false>
 __device__ __forceinline__ bool kwait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
   if constexpr (kOut) {
@@ -384,7 +385,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
                       const __grid_constant__ CUtensorMap kv_map_r,
                       const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap out_map,
                       const __grid_constant__ CUtensorMap out_map4, const DecodeArgs a) {
-  constexpr bool kOutWait = kFp8 && !kRopeB;  // see kwait
+  // see kwait: fp8 variant A takes every waiting loop out of line; bf16 the
+  // loops of waits outside the per-page loops (segment ends, epilogue, merge)
+  constexpr bool kOutWait = kFp8 && !kRopeB;
+  constexpr bool kOutCold = !(kFp8 && kRopeB);
   constexpr int kStagesA = AccLayout<kFp8>::kStagesA, kPBufs = AccLayout<kFp8>::kPBufs;
   constexpr int kOffP = AccLayout<kFp8>::kOffP, kOffAlpha = AccLayout<kFp8>::kOffAlpha, kOffL = AccLayout<kFp8>::kOffL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
           int pid = __shfl_sync(0xffffffffu, my_pid, k);
           if (lane == 0 && wait_first_p) {
             wait_first_p = false;
-            if (!kwait<kOutWait, true>(smem_u32(&bars->p_full[0]), 0u, abort_flag)) {
+            if (!kwait<kOutCold, true>(smem_u32(&bars->p_full[0]), 0u, abort_flag)) {
               ok = false;
               if (!*abort_flag) signal_abort(bars, a.err, peer);
             }
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       // wait (time-bounded only) for the loads already in flight
       for (int i = 0; i < nst; ++i)
         if (last_par[i] >= 0)
-          kwait<kOutWait>(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
+          kwait<kOutCold>(smem_u32(kFp8 ? &bars->raw_full[i] : &bars->kv_full[i]), static_cast<uint32_t>(last_par[i]), nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -607,7 +611,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
     if (scorer && __ldg(a.hdr + kHdrStall) != 0) {
       // a test's stall request: wait on a barrier nothing signals, so the
       // bounded wait runs out and the whole cluster takes its abort path
-      if (!kwait<kOutWait>(smem_u32(&bars->stall), 0u, abort_flag)) ok = false;
+      if (!kwait<kOutCold>(smem_u32(&bars->stall), 0u, abort_flag)) ok = false;
     }
     if (scorer) {
       // S = Q K^T: 36 steps of K=16 over the 576 channels, A = Q in TMEM.
@@ -628,7 +632,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       uint32_t sgp = 0;
       while (ok && it.next(s)) {
         if (s.empty) continue;
-        if (!kwait<kOutWait>(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
+        if (!kwait<kOutCold>(smem_u32(&bars->q_full), q_ph, abort_flag)) { ok = false; break; }
         q_ph ^= 1u;
         if (!kFp8) {
           // Q is in TMEM, so the two stages that brought it are free
@@ -729,7 +733,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
           }
           if (!kwait<kOutWait>(smem_u32(&bars->corr_done[sb]), (t / kPBufs) & 1u, abort_flag)) { ok = false; break; }
           if (j == s.page_lo) {
-            if (!kwait<kOutWait>(smem_u32(&bars->o_free), ofree_ph ^ 1u, abort_flag)) { ok = false; break; }
+            if (!kwait<kOutCold>(smem_u32(&bars->o_free), ofree_ph ^ 1u, abort_flag)) { ok = false; break; }
             ofree_ph ^= 1u;
           }
           tc_fence_after();
@@ -762,7 +766,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
     if (!ok && !*abort_flag && lane == 0) signal_abort(bars, a.err, peer);
     if (lane == 0) {
       mma_commit(smem_u32(&bars->drain));
-      kwait<kOutWait>(smem_u32(&bars->drain), 0u, nullptr);
+      kwait<kOutCold>(smem_u32(&bars->drain), 0u, nullptr);
     }
     __syncwarp();
   } else if (warp < 6 || (!kFp8 && scorer)) {
@@ -808,7 +812,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       auto load_q_ring = [&](uint32_t r0) -> bool {
         const uint32_t rq = r0 + (L >= 64 ? 1u : 0u);
         const uint32_t st = rq % kStages;
-        if (!kwait<kOutWait>(smem_u32(&bars->kv_full[st]), (rq / kStages) & 1u, abort_flag)) return false;
+        if (!kwait<kOutCold>(smem_u32(&bars->kv_full[st]), (rq / kStages) & 1u, abort_flag)) return false;
         const uint8_t* qs_base = smem + st * kStageS;
         const int row = L & 63;
         for (int c = hh ? 5 : 0; c < (hh ? 9 : 5); ++c) {
@@ -916,7 +920,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       auto exchange = [&](float v, float& other) -> bool {
         xchg[((xph & 1u) * 2 + hh) * kRowsPerBlock + L] = v;
         mbar_arrive(smem_u32(&bars->mx_bar[wq]));
-        const bool done = kwait<kOutWait>(smem_u32(&bars->mx_bar[wq]), xph & 1u, abort_flag);
+        const bool done = kwait<kOutCold>(smem_u32(&bars->mx_bar[wq]), xph & 1u, abort_flag);
         other = xchg[((xph & 1u) * 2 + (hh ^ 1)) * kRowsPerBlock + L];
         ++xph;
         return done;
@@ -1141,7 +1145,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         if (hh == 0 && !fwd) {
           // the row sum and lse go to the accumulator, which writes the outputs
           const float lse_v = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
-          if (!kwait<kOutWait>(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          if (!kwait<kOutCold>(smem_u32(&bars->l_free), (seg_n & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           st_async_v2_f32(rL + L * 8, l, lse_v, rLfull);
           ++seg_n;
         }
@@ -1173,7 +1177,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
       uint32_t ofull_ph = 0, epi_ph = 0, mrg_n = 0;
       auto epi_sync = [&]() -> bool {
         mbar_arrive(smem_u32(&bars->epi_bar));
-        const bool done = kwait<kOutWait>(smem_u32(&bars->epi_bar), epi_ph, abort_flag);
+        const bool done = kwait<kOutCold>(smem_u32(&bars->epi_bar), epi_ph, abort_flag);
         epi_ph ^= 1u;
         return done;
       };
@@ -1237,10 +1241,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
         //  2  the last piece to finish of a unit with at most kFuseMax pieces:
         //     merges the other pieces' partials with its own O (the LSE merge)
         //     and writes out and lse itself.
-        if (!kwait<kOutWait>(smem_u32(&bars->o_full), ofull_ph, abort_flag)) { ok = false; break; }
+        if (!kwait<kOutCold>(smem_u32(&bars->o_full), ofull_ph, abort_flag)) { ok = false; break; }
         ofull_ph ^= 1u;
         if (ctid == 0) mbar_arrive_expect_tx(smem_u32(&bars->l_full), kRowsPerBlock * 8);
-        if (!kwait<kOutWait, true>(smem_u32(&bars->l_full), seg_n & 1u, abort_flag)) { ok = false; break; }
+        if (!kwait<kOutCold, true>(smem_u32(&bars->l_full), seg_n & 1u, abort_flag)) { ok = false; break; }
         const float2 lrow = l_s[L];  // (row sum, lse) of this piece
         ++seg_n;
         const float l = lrow.x, lse_own = lrow.y;
@@ -1383,7 +1387,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kRopeB>::kThreads, 1)
                 for (int off = 0; off < kPartBytes; off += 32768)
                   bulk_load(smem_u32(smem + off), reinterpret_cast<const uint8_t*>(gsrc) + off, 32768, mb);
               }
-              if (!kwait<kOutWait>(smem_u32(&bars->mrg_bar), mrg_n & 1u, abort_flag)) { ok = false; break; }
+              if (!kwait<kOutCold>(smem_u32(&bars->mrg_bar), mrg_n & 1u, abort_flag)) { ok = false; break; }
               ++mrg_n;
               src = reinterpret_cast<const uint4*>(smem) + L;
             }
